@@ -1,0 +1,185 @@
+/*
+ * moe.h -- C ABI of the B300 (sm_103a) top-k Mixture-of-Experts layer forward.
+ *
+ * The layer, as the "Mixture of Experts" lesson of AI Engineering from Scratch
+ * (Phase 07, section "Concept") writes it:
+ *
+ *     scores = router(norm(h))                       (N tokens x E experts)
+ *     top_k  = argmax_k(scores + bias)               (bias picks, never weighs)
+ *     out    = h + shared(norm(h)) + sum_{e in top_k} gate_e * Expert_e(norm(h))
+ *
+ * with every expert a SwiGLU FFN.  The five calls below run it step by step:
+ * router + top-k + gates, histogram + scan + permute, grouped SwiGLU GEMMs,
+ * un-permute + gated combine, and the +-gamma bias step.
+ *
+ * Conventions shared by every call
+ *  - Pointers are DEVICE pointers owned by the caller unless a parameter says
+ *    otherwise.  The library never allocates device memory; scratch space is
+ *    passed in by the caller.
+ *  - Arrays are dense, row-major, and 16-byte aligned.
+ *  - Every call is asynchronous on `stream` and returns a moe_status_t.  Host-side
+ *    argument checks return MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED before
+ *    anything is launched; a launch failure returns MOE_ERR_CUDA.  Faults detected
+ *    on the device (a pipeline wait that exceeded its time limit, an expert id out
+ *    of range) are recorded in a per-device status word, read by
+ *    moe_last_device_status().  No call traps or aborts.
+ *  - Results are deterministic: the same inputs give the same bits, run to run.
+ */
+#ifndef MOE_B300_H
+#define MOE_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+typedef enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = -1, /* null/unaligned pointer, size out of range, bad id */
+  MOE_ERR_UNSUPPORTED = -2, /* shape or dtype this build does not run */
+  MOE_ERR_CUDA = -3,        /* a CUDA runtime call or kernel launch failed */
+  MOE_ERR_TIMEOUT = -4,     /* a device-side wait gave up (status word) */
+  MOE_ERR_NAN_INPUT = -5    /* reserved for input screening */
+} moe_status_t;
+
+typedef enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype_t;
+
+/* Score function of the router.
+ *  MOE_SCORE_SOFTMAX: selection on logit + bias; gates = softmax over the k chosen
+ *    raw logits (lesson, "Build it", step 1).
+ *  MOE_SCORE_SIGMOID: s = sigmoid(logit); selection on s + bias; gates = s_j / sum of
+ *    the chosen s (the sigmoid router the handbook article names, read this way). */
+typedef enum moe_score_fn { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 } moe_score_fn_t;
+
+/* Largest E the router/top-k kernel handles, and largest k. */
+#define MOE_MAX_EXPERTS 256
+#define MOE_MAX_TOPK 16
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* moe_status_string(moe_status_t status);
+
+/* Waits for `stream`, then returns and clears the status word of the current device:
+ * MOE_OK, MOE_ERR_TIMEOUT (a pipeline wait gave up) or MOE_ERR_INVALID_ARG (an
+ * expert id outside [0, E) reached moe_permute). */
+moe_status_t moe_last_device_status(moe_stream_t stream);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int moe_version(void);
+
+/*
+ * moe_router_topk -- router GEMM, score function, biased top-k and gates.
+ * Lesson "Build it" step 1 (router) and "Load-balancing problem" item 3 (the bias
+ * changes which experts are chosen, never their gate weights); handbook article,
+ * router-precision paragraph (the router runs in fp32).
+ *
+ *   xn        [N, D]  activations (norm(h)), MOE_BF16 or MOE_F32 (x_dtype)
+ *   w_router  [E, D]  fp32 router weight
+ *   bias      [E]     fp32 selection bias, or NULL for zero bias
+ *   logits_out[N, E]  fp32 logits = xn . w_router^T, or NULL to skip writing them
+ *   topk_idx  [N, k]  int32 chosen expert ids, in descending selection score; equal
+ *                     scores are ordered by ascending id; NaN scores rank last
+ *   topk_gate [N, k]  fp32 gate weights (sum to 1 per token)
+ *   near_tie  [N]     uint8: 1 when the k-th and (k+1)-th selection scores differ by
+ *                     less than 1e-6 (0 when k == E), or NULL
+ * Requires 1 <= k <= min(E, 16), 1 <= E <= 256, D % 64 == 0, N >= 0.
+ * Logits are accumulated in fp32 with per-32-element partial sums combined by
+ * compensated (two-sum) addition.
+ */
+moe_status_t moe_router_topk(const void* xn, moe_dtype_t x_dtype, int N, int D,
+                             const float* w_router, const float* bias, int E, int k,
+                             moe_score_fn_t fn, float* logits_out, int32_t* topk_idx,
+                             float* topk_gate, uint8_t* near_tie, moe_stream_t stream);
+
+/* Bytes of scratch moe_permute needs for (N, k, E). */
+size_t moe_permute_workspace_bytes(int N, int k, int E);
+
+/*
+ * moe_permute -- per-expert histogram, exclusive scan and stable permutation.
+ * Lesson "Build it" step 2 (count how often each expert fires) and the evaluation
+ * article's per-expert routed-token histogram; the permutation groups each expert's
+ * tokens into one contiguous block of rows for the grouped GEMM.
+ *
+ *   xn         [N, D]  rows to permute (dtype), or NULL together with x_perm
+ *   topk_idx   [N, k]  int32 expert ids in [0, E) (from moe_router_topk, or replayed)
+ *   counts     [E]     int32 out: number of (token, slot) pairs per expert
+ *   offsets    [E + 1] int32 out: exclusive scan of counts; offsets[E] = N*k
+ *   row_map    [N, k]  int32 out: permuted row of slot (n, j), or NULL
+ *   perm_token [N*k]   int32 out: token of each permuted row, or NULL
+ *   x_perm     [N*k, D] out: x_perm[row_map[n, j]] = xn[n], or NULL
+ *   workspace  scratch of at least moe_permute_workspace_bytes(N, k, E) bytes
+ * Rows of expert e occupy [offsets[e], offsets[e+1]) in slot order n*k + j (stable).
+ * row_map and perm_token must be both given or both NULL; x_perm needs them.
+ * An id outside [0, E) sets MOE_ERR_INVALID_ARG in the status word and is skipped.
+ */
+moe_status_t moe_permute(const void* xn, moe_dtype_t dtype, int N, int D,
+                         const int32_t* topk_idx, int k, int E, int32_t* counts,
+                         int32_t* offsets, int32_t* row_map, int32_t* perm_token,
+                         void* x_perm, void* workspace, size_t workspace_bytes,
+                         moe_stream_t stream);
+
+/*
+ * moe_grouped_swiglu -- every expert's SwiGLU FFN on its block of permuted rows.
+ * Lesson "Concept" (each expert an independent SwiGLU FFN) and "Shared experts"
+ * (call with G = 1 and offsets = {0, N} on xn for the always-on expert).
+ *
+ *   x_perm      [M_total, D]  rows grouped by expert (dtype)
+ *   offsets     [G + 1]       DEVICE int32, non-decreasing, offsets[0] = 0,
+ *                             offsets[G] <= M_total; rows of group g are
+ *                             [offsets[g], offsets[g+1])
+ *   w_gate,w_up [G, F, D]     gate and up projections (PyTorch Linear layout)
+ *   w_down      [G, D, F]     down projection
+ *   h_workspace [M_total, F]  scratch for H = SiLU(x W_gate^T) * (x W_up^T)
+ *   y_perm      [M_total, D]  out: H W_down^T per row (rows past offsets[G] untouched)
+ * MOE_BF16: tcgen05 tensor-core kernels, fp32 accumulation in tensor memory, H and Y
+ *           rounded to bf16.  MOE_F32: CUDA-core fp32 kernels.
+ * Requires D % 64 == 0, F % 64 == 0, 1 <= G.
+ */
+moe_status_t moe_grouped_swiglu(const void* x_perm, moe_dtype_t dtype, const int32_t* offsets,
+                                int G, int M_total, int D, int F, const void* w_gate,
+                                const void* w_up, const void* w_down, void* h_workspace,
+                                void* y_perm, moe_stream_t stream);
+
+/*
+ * moe_unpermute_combine -- gather each token's k expert outputs and mix them.
+ * Lesson "Concept": out = h + sum_j gate_j * Expert_j(norm(h)), plus the shared
+ * expert's output with weight 1 ("Shared experts").
+ *
+ *   y_perm    [N*k, D]  expert outputs in permuted row order (dtype)
+ *   row_map   [N, k]    int32 from moe_permute
+ *   topk_gate [N, k]    fp32 gates
+ *   shared_y  [N, D]    shared-expert output (dtype) or NULL
+ *   residual  [N, D]    h (dtype) or NULL
+ *   out       [N, D]    out (dtype)
+ * The sum runs in fp32 in slot order j = 0..k-1, then adds shared_y and residual,
+ * and is rounded once to dtype.
+ */
+moe_status_t moe_unpermute_combine(const void* y_perm, const int32_t* row_map,
+                                   const float* topk_gate, int N, int k, int D,
+                                   const void* shared_y, const void* residual, void* out,
+                                   moe_dtype_t dtype, moe_stream_t stream);
+
+/*
+ * moe_bias_update -- the auxiliary-loss-free +-gamma step.
+ * Lesson "Load-balancing problem" item 3 and "Build it" step 2: after a step, each
+ * expert whose load is above the uniform target moves down by gamma, each below it
+ * moves up by gamma:  bias[e] += gamma * sign(total/E - counts[e])  (sign(0) = 0),
+ * evaluated exactly on integers and added in fp32.
+ *
+ *   counts            [E] int32 per-expert loads of the step (from moe_permute)
+ *   total_assignments N*k of that step
+ *   bias              [E] fp32, updated in place
+ *   max_over_mean_out [1] fp32 out: max(counts) / (total/E), or NULL
+ */
+moe_status_t moe_bias_update(const int32_t* counts, int E, int64_t total_assignments,
+                             float gamma, float* bias, float* max_over_mean_out,
+                             moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_B300_H */

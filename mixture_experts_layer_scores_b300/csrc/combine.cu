@@ -1,0 +1,146 @@
+// Un-permute + gate-weighted combine, and the +-gamma bias step.
+//
+// Lesson "Mixture of Experts", section "Concept": out = h + sum_j gate_j * Expert_j(x),
+// "Shared experts": the always-on expert adds its output with weight 1.
+// "Load-balancing problem" item 3 and "Build it" step 2: each expert's bias moves by
+// gamma against the sign of its load error.
+#include "moe_internal.cuh"
+
+namespace moe {
+namespace {
+
+template <typename T>
+struct Vec;  // one 16-byte vector of T as floats
+
+template <>
+struct Vec<__nv_bfloat16> {
+  static constexpr int W = 8;
+  __device__ static void load(const void* p, float* f) {
+    bf16x8_to_f32(__ldg(static_cast<const uint4*>(p)), f);
+  }
+  __device__ static void store(void* p, const float* f) {
+    *static_cast<uint4*>(p) = f32_to_bf16x8(f);
+  }
+};
+
+template <>
+struct Vec<float> {
+  static constexpr int W = 4;
+  __device__ static void load(const void* p, float* f) {
+    const float4 v = __ldg(static_cast<const float4*>(p));
+    f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
+  }
+  __device__ static void store(void* p, const float* f) {
+    *static_cast<float4*>(p) = make_float4(f[0], f[1], f[2], f[3]);
+  }
+};
+
+// One block per token; threads stride over the row's 16-byte vectors.
+template <typename T>
+__global__ void __launch_bounds__(128) combine_kernel(const T* __restrict__ y, const int32_t* __restrict__ row_map,
+                                                      const float* __restrict__ gate, int k, int D,
+                                                      const T* __restrict__ shared_y,
+                                                      const T* __restrict__ residual, T* __restrict__ out) {
+  constexpr int W = Vec<T>::W;
+  const int n = blockIdx.x;
+  __shared__ int rows[MOE_MAX_TOPK];
+  __shared__ float gs[MOE_MAX_TOPK];
+  if (threadIdx.x < k) {
+    rows[threadIdx.x] = row_map[(size_t)n * k + threadIdx.x];
+    gs[threadIdx.x] = gate[(size_t)n * k + threadIdx.x];
+  }
+  __syncthreads();
+  const int V = D / W;
+  for (int c = threadIdx.x; c < V; c += blockDim.x) {
+    float acc[W];
+#pragma unroll
+    for (int i = 0; i < W; ++i) acc[i] = 0.f;
+    for (int j = 0; j < k; ++j) {
+      const int r = rows[j];
+      if (r < 0) continue;
+      float f[W];
+      Vec<T>::load(y + (size_t)r * D + c * W, f);
+      const float g = gs[j];
+#pragma unroll
+      for (int i = 0; i < W; ++i) acc[i] = fmaf(g, f[i], acc[i]);
+    }
+    if (shared_y) {
+      float f[W];
+      Vec<T>::load(shared_y + (size_t)n * D + c * W, f);
+#pragma unroll
+      for (int i = 0; i < W; ++i) acc[i] += f[i];
+    }
+    if (residual) {
+      float f[W];
+      Vec<T>::load(residual + (size_t)n * D + c * W, f);
+#pragma unroll
+      for (int i = 0; i < W; ++i) acc[i] += f[i];
+    }
+    Vec<T>::store(out + (size_t)n * D + c * W, acc);
+  }
+}
+
+__global__ void bias_update_kernel(const int32_t* __restrict__ counts, int E, long long total,
+                                   float gamma, float* __restrict__ bias, float* __restrict__ mom) {
+  __shared__ int smax[32];
+  int m = 0;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const long long c = counts[e];
+    const long long d = total - (long long)E * c;  // sign(total/E - c), exactly
+    const float sg = d > 0 ? 1.f : (d < 0 ? -1.f : 0.f);
+    bias[e] = bias[e] + gamma * sg;
+    m = max(m, (int)c);
+  }
+  if (mom) {
+    for (int off = 16; off > 0; off >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, off));
+    if ((threadIdx.x & 31) == 0) smax[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int mm = 0;
+      for (int w = 0; w < (int)(blockDim.x + 31) / 32; ++w) mm = max(mm, smax[w]);
+      *mom = total > 0 ? (float)((double)mm * E / (double)total) : 0.f;
+    }
+  }
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" moe_status_t moe_unpermute_combine(const void* y_perm, const int32_t* row_map,
+                                              const float* topk_gate, int N, int k, int D,
+                                              const void* shared_y, const void* residual, void* out,
+                                              moe_dtype_t dtype, moe_stream_t stream) {
+  using namespace moe;
+  if (N < 0 || k < 1 || D <= 0) return MOE_ERR_INVALID_ARG;
+  if (k > MOE_MAX_TOPK) return MOE_ERR_UNSUPPORTED;
+  if (dtype != MOE_BF16 && dtype != MOE_F32) return MOE_ERR_UNSUPPORTED;
+  const int esize = dtype == MOE_BF16 ? 2 : 4;
+  if ((D * esize) % 16 != 0) return MOE_ERR_UNSUPPORTED;
+  if (N == 0) return MOE_OK;
+  if (!y_perm || !row_map || !topk_gate || !out) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(y_perm) || !aligned16(out) || (shared_y && !aligned16(shared_y)) ||
+      (residual && !aligned16(residual)))
+    return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = as_cuda(stream);
+  if (dtype == MOE_BF16)
+    combine_kernel<__nv_bfloat16><<<N, 128, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(y_perm), row_map, topk_gate, k, D,
+        static_cast<const __nv_bfloat16*>(shared_y), static_cast<const __nv_bfloat16*>(residual),
+        static_cast<__nv_bfloat16*>(out));
+  else
+    combine_kernel<float><<<N, 128, 0, s>>>(static_cast<const float*>(y_perm), row_map, topk_gate, k, D,
+                                            static_cast<const float*>(shared_y),
+                                            static_cast<const float*>(residual), static_cast<float*>(out));
+  return launch_status();
+}
+
+extern "C" moe_status_t moe_bias_update(const int32_t* counts, int E, int64_t total_assignments,
+                                        float gamma, float* bias, float* max_over_mean_out,
+                                        moe_stream_t stream) {
+  using namespace moe;
+  if (E < 1 || total_assignments < 0 || !counts || !bias) return MOE_ERR_INVALID_ARG;
+  if (E > 1 << 20) return MOE_ERR_UNSUPPORTED;
+  bias_update_kernel<<<1, 1024, 0, as_cuda(stream)>>>(counts, E, (long long)total_assignments, gamma,
+                                                      bias, max_over_mean_out);
+  return launch_status();
+}

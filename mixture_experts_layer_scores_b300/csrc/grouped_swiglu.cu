@@ -1,0 +1,550 @@
+// Grouped SwiGLU expert FFN over ragged per-expert row blocks.
+//
+// Lesson "Mixture of Experts", section "Concept": every expert is an independent
+// SwiGLU FFN, y = W_down (SiLU(W_gate x) * (W_up x)); section "Shared experts": the
+// always-on expert is the same computation with one group covering every token.
+//
+// bf16 path: two launches of one persistent, warp-specialised tcgen05 kernel.
+//   GEMM1  acc[128 x 256] = X[rows] . [W_gate[n0:n0+128] ; W_up[n0:n0+128]]^T
+//          epilogue H = SiLU(acc[:, :128]) * acc[:, 128:]  -> bf16
+//   GEMM2  acc[128 x 256] = H[rows] . W_down[n0:n0+256]^T  -> bf16 Y
+// Roles (192 threads, one CTA per SM):
+//   warp 0      one lane issues TMA loads (128B-swizzled K-major tiles) into a
+//               4-stage shared-memory ring guarded by full/empty mbarriers;
+//   warp 1      allocates 512 TMEM columns (two 256-column fp32 accumulators) and
+//               one lane issues tcgen05.mma (M=128, N=256, K=16) and tcgen05.commit;
+//   warps 2..5  drain an accumulator with tcgen05.ld while the MMA warp fills the
+//               other one, apply the epilogue and store bf16 rows, masking rows past
+//               the expert's segment and columns past the output width.
+// Tiles are (expert g, column block, 128-row block) with the row block fastest, so
+// CTAs running at the same time share weight tiles through L2.  The tile list comes
+// from the device-side offsets: every CTA scans them into shared memory at start.
+// Every mbarrier wait is bounded in wall time; on expiry the kernel records
+// MOE_ERR_TIMEOUT in the status word, lets in-flight copies and MMAs land, frees
+// its TMEM and returns.
+//
+// fp32 path: plain CUDA-core kernels (one thread per output element).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "moe_internal.cuh"
+
+namespace moe {
+namespace tc {
+
+constexpr int BM = 128;                 // rows per tile (UMMA M)
+constexpr int BN = 256;                 // accumulator columns (UMMA N)
+constexpr int BK = 64;                  // K per stage: one 128-byte swizzle row of bf16
+constexpr int UK = 16;                  // K per tcgen05.mma (bf16)
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;    // 16 KB
+constexpr int B_BYTES = BN * BK * 2;    // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int THREADS = 192;
+constexpr int TMEM_COLS = 512;
+constexpr int MAX_GROUPS = 1024;
+constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;  // 2 s
+
+// kind::f16 instruction descriptor: D = f32, A = B = bf16, both K-major, N = 256, M = 128.
+constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                           ((uint32_t)(BM >> 4) << 24);
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long now_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait.  Returns false if the kernel is aborting (honour_abort) or the wait
+// exceeded WAIT_LIMIT_NS, in which case it raises the abort flag and the status word.
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                       int* status, bool honour_abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = now_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (honour_abort && *abort_flag) return false;
+      if (now_ns() - t0 > WAIT_LIMIT_NS) {
+        *abort_flag = 1;
+        atomicOr(status, kStatusTimeout);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);  // start address
+  d |= (uint64_t)1 << 16;                    // leading byte offset (unused with swizzle)
+  d |= (uint64_t)(1024 >> 4) << 32;          // stride byte offset
+  d |= (uint64_t)1 << 46;                    // descriptor version
+  d |= (uint64_t)2 << 61;                    // 128-byte swizzle
+  return d;
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accum) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(IDESC), "r"(accum)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+        "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+        "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+struct Tile {
+  int g, row0, rows, nb;
+};
+
+__device__ __forceinline__ Tile decode(int tile, const int* tile_start, int G, const int32_t* offsets,
+                                       int M_total, int NB) {
+  int lo = 0, hi = G - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (tile_start[mid] <= tile) lo = mid; else hi = mid - 1;
+  }
+  Tile t;
+  t.g = lo;
+  const int s = min(max(__ldg(offsets + lo), 0), M_total);
+  const int e = min(max(__ldg(offsets + lo + 1), s), M_total);
+  const int mblk = (e - s + BM - 1) / BM;
+  const int local = tile - tile_start[lo];
+  t.nb = local / mblk;
+  const int mb = local - t.nb * mblk;
+  t.row0 = s + mb * BM;
+  t.rows = min(BM, e - t.row0);
+  return t;
+}
+
+// MODE 0: GEMM1 with SwiGLU epilogue (B = gate rows ; up rows, 128 output columns per tile)
+// MODE 1: GEMM2 (B = 256 rows of W_down, 256 output columns per tile)
+template <int MODE>
+__global__ void __launch_bounds__(THREADS, 1)
+grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b0,
+                    const __grid_constant__ CUtensorMap map_b1, const int32_t* __restrict__ offsets,
+                    int G, int M_total, int K, int NOUT, __nv_bfloat16* __restrict__ out,
+                    int* __restrict__ status) {
+  constexpr int TN = MODE == 0 ? BN / 2 : BN;  // output columns per tile
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], done
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  int* wtot = reinterpret_cast<int*>(tmem_holder + 2);  // [8]
+  int* tile_start = wtot + 8;                            // [G + 1]
+
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int NB = (NOUT + TN - 1) / TN;
+  const int KB = K / BK;
+  auto full_bar = [&](int s) { return smem_u32(bars + s); };
+  auto empty_bar = [&](int s) { return smem_u32(bars + STAGES + s); };
+  auto tfull_bar = [&](int a) { return smem_u32(bars + 2 * STAGES + a); };
+  auto tempty_bar = [&](int a) { return smem_u32(bars + 2 * STAGES + 2 + a); };
+  const uint32_t done_bar = smem_u32(bars + 2 * STAGES + 4);
+
+  if (t == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 128);
+    }
+    mbar_init(done_bar, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_holder)),
+                 "r"(TMEM_COLS));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  if (warp == 0 && lane == 0) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_a)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_b0)) : "memory");
+    if (MODE == 0) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_b1)) : "memory");
+  }
+
+  // tile_start[g] = sum over g' < g of (row blocks of g') * NB
+  {
+    const int per = (G + THREADS - 1) / THREADS;
+    const int g0 = min(G, t * per), g1 = min(G, g0 + per);
+    int local = 0;
+    for (int g = g0; g < g1; ++g) {
+      const int s = min(max(__ldg(offsets + g), 0), M_total);
+      const int e = min(max(__ldg(offsets + g + 1), s), M_total);
+      local += ((e - s + BM - 1) / BM) * NB;
+    }
+    int incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += y;
+    }
+    if (lane == 31) wtot[warp] = incl;
+    __syncthreads();
+    int base = 0;
+    for (int w = 0; w < warp; ++w) base += wtot[w];
+    base += incl - local;
+    for (int g = g0; g < g1; ++g) {
+      tile_start[g] = base;
+      const int s = min(max(__ldg(offsets + g), 0), M_total);
+      const int e = min(max(__ldg(offsets + g + 1), s), M_total);
+      base += ((e - s + BM - 1) / BM) * NB;
+    }
+    if (t == THREADS - 1) {
+      int tot = 0;
+      for (int w = 0; w < THREADS / 32; ++w) tot += wtot[w];
+      tile_start[G] = tot;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  const int total_tiles = tile_start[G];
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer ----------------
+      int stage = 0;
+      uint32_t phase = 0, issued = 0, issued_par = 0;
+      for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+        const Tile tl = decode(tile, tile_start, G, offsets, M_total, NB);
+        const int brow = MODE == 0 ? tl.g * NOUT + tl.nb * TN : tl.g * NOUT + tl.nb * TN;
+        bool ok = true;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, status, true)) { ok = false; break; }
+          const uint32_t a_dst = smem_u32(smem + stage * STAGE_BYTES);
+          const uint32_t b_dst = a_dst + A_BYTES;
+          mbar_expect_tx(full_bar(stage), STAGE_BYTES);
+          tma_load_2d(a_dst, &map_a, kb * BK, tl.row0, full_bar(stage));
+          if (MODE == 0) {
+            tma_load_2d(b_dst, &map_b0, kb * BK, brow, full_bar(stage));
+            tma_load_2d(b_dst + B_BYTES / 2, &map_b1, kb * BK, brow, full_bar(stage));
+          } else {
+            tma_load_2d(b_dst, &map_b0, kb * BK, brow, full_bar(stage));
+          }
+          issued |= 1u << stage;
+          issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+      }
+      // let every issued copy land before the CTA can exit
+      for (int s = 0; s < STAGES; ++s)
+        if ((issued >> s) & 1u) mbar_wait(full_bar(s), (issued_par >> s) & 1u, abort_flag, status, false);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+        if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, status, true)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        bool ok = true;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(full_bar(stage), phase, abort_flag, status, true)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(smem + stage * STAGE_BYTES);
+          const uint32_t b_base = a_base + A_BYTES;
+#pragma unroll
+          for (int k = 0; k < BK / UK; ++k)
+            tc_mma(d_tmem, sw128_desc(a_base + k * UK * 2), sw128_desc(b_base + k * UK * 2),
+                   (kb | k) != 0 ? 1u : 0u);
+          tc_commit(empty_bar(stage));
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        tc_commit(tfull_bar(acc));
+        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+      }
+      // every MMA issued so far completes before TMEM is freed
+      tc_commit(done_bar);
+      mbar_wait(done_bar, 0, abort_flag, status, false);
+    }
+  } else {
+    // ---------------- epilogue (warps 2..5) ----------------
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int row_local = q * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+      const Tile tl = decode(tile, tile_start, G, offsets, M_total, NB);
+      const bool ok = mbar_wait(tfull_bar(acc), acc_phase, abort_flag, status, true);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+      const bool valid = row_local < tl.rows;
+      __nv_bfloat16* orow = out + (size_t)(tl.row0 + row_local) * NOUT + tl.nb * TN;
+      if (MODE == 0) {
+#pragma unroll 1
+        for (int c = 0; c < TN / 32; ++c) {
+          uint32_t gv[32], uv[32];
+          tmem_ld32(taddr + c * 32, gv);
+          tmem_ld32(taddr + TN + c * 32, uv);
+          tmem_ld_wait();
+          if (valid && tl.nb * TN + c * 32 < NOUT) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              float h[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const float g = __uint_as_float(gv[v * 8 + i]);
+                const float u = __uint_as_float(uv[v * 8 + i]);
+                h[i] = (g / (1.0f + __expf(-g))) * u;
+              }
+              dst[v] = f32_to_bf16x8(h);
+            }
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < TN / 32; ++c) {
+          uint32_t yv[32];
+          tmem_ld32(taddr + c * 32, yv);
+          tmem_ld_wait();
+          if (valid && tl.nb * TN + c * 32 < NOUT) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              float y[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) y[i] = __uint_as_float(yv[v * 8 + i]);
+              dst[v] = f32_to_bf16x8(y);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(tempty_bar(acc));
+      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS));
+  }
+}
+
+// ---- host: tensor maps ---------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2D bf16 row-major [rows, cols] -> box {64 cols, box_rows}, 128-byte swizzle
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+size_t smem_bytes(int G) { return 1024 + (size_t)STAGES * STAGE_BYTES + 256 + (size_t)(G + 16) * 4; }
+
+template <int MODE>
+moe_status_t launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1, const int32_t* offsets,
+                    int G, int M_total, int K, int NOUT, void* out, int* status, cudaStream_t s) {
+  const size_t smem = smem_bytes(G);
+  auto kern = grouped_gemm_kernel<MODE>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  const int TN = MODE == 0 ? BN / 2 : BN;
+  const long long NB = (NOUT + TN - 1) / TN;
+  const long long max_tiles = ((long long)(M_total + BM - 1) / BM + G) * NB;
+  const int grid = (int)std::min<long long>(max_tiles, (long long)sm_count());
+  kern<<<grid, THREADS, smem, s>>>(a, b0, b1, offsets, G, M_total, K, NOUT,
+                                   static_cast<__nv_bfloat16*>(out), status);
+  return launch_status();
+}
+
+}  // namespace tc
+
+namespace simt {
+
+__global__ void swiglu_up_kernel(const float* __restrict__ x, const int32_t* __restrict__ offsets, int G,
+                                 int M, int D, int F, const float* __restrict__ wg,
+                                 const float* __restrict__ wu, float* __restrict__ h) {
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (long long)M * F) return;
+  const int r = (int)(i / F), f = (int)(i % F);
+  int lo = 0, hi = G - 1;  // group of row r: largest g with offsets[g] <= r
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (offsets[mid] <= r) lo = mid; else hi = mid - 1;
+  }
+  if (r < offsets[lo] || r >= offsets[lo + 1]) return;
+  const float* xr = x + (size_t)r * D;
+  const float* gr = wg + ((size_t)lo * F + f) * D;
+  const float* ur = wu + ((size_t)lo * F + f) * D;
+  float a = 0.f, b = 0.f;
+  for (int d = 0; d < D; d += 4) {
+    const float4 xv = *reinterpret_cast<const float4*>(xr + d);
+    const float4 gv = *reinterpret_cast<const float4*>(gr + d);
+    const float4 uv = *reinterpret_cast<const float4*>(ur + d);
+    a = fmaf(xv.x, gv.x, a); a = fmaf(xv.y, gv.y, a); a = fmaf(xv.z, gv.z, a); a = fmaf(xv.w, gv.w, a);
+    b = fmaf(xv.x, uv.x, b); b = fmaf(xv.y, uv.y, b); b = fmaf(xv.z, uv.z, b); b = fmaf(xv.w, uv.w, b);
+  }
+  h[(size_t)r * F + f] = (a / (1.0f + expf(-a))) * b;
+}
+
+__global__ void swiglu_down_kernel(const float* __restrict__ h, const int32_t* __restrict__ offsets, int G,
+                                   int M, int D, int F, const float* __restrict__ wd, float* __restrict__ y) {
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (long long)M * D) return;
+  const int r = (int)(i / D), d = (int)(i % D);
+  int lo = 0, hi = G - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (offsets[mid] <= r) lo = mid; else hi = mid - 1;
+  }
+  if (r < offsets[lo] || r >= offsets[lo + 1]) return;
+  const float* hr = h + (size_t)r * F;
+  const float* wr = wd + ((size_t)lo * D + d) * F;
+  float a = 0.f;
+  for (int f = 0; f < F; f += 4) {
+    const float4 hv = *reinterpret_cast<const float4*>(hr + f);
+    const float4 wv = *reinterpret_cast<const float4*>(wr + f);
+    a = fmaf(hv.x, wv.x, a); a = fmaf(hv.y, wv.y, a); a = fmaf(hv.z, wv.z, a); a = fmaf(hv.w, wv.w, a);
+  }
+  y[(size_t)r * D + d] = a;
+}
+
+}  // namespace simt
+}  // namespace moe
+
+extern "C" moe_status_t moe_grouped_swiglu(const void* x_perm, moe_dtype_t dtype, const int32_t* offsets,
+                                           int G, int M_total, int D, int F, const void* w_gate,
+                                           const void* w_up, const void* w_down, void* h_workspace,
+                                           void* y_perm, moe_stream_t stream) {
+  using namespace moe;
+  if (G < 1 || M_total < 0 || D <= 0 || F <= 0) return MOE_ERR_INVALID_ARG;
+  if (D % 64 != 0 || F % 64 != 0 || G > tc::MAX_GROUPS) return MOE_ERR_UNSUPPORTED;
+  if (dtype != MOE_BF16 && dtype != MOE_F32) return MOE_ERR_UNSUPPORTED;
+  if ((long long)G * F >= (1LL << 31) || (long long)G * D >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
+  if (M_total == 0) return MOE_OK;
+  if (!x_perm || !offsets || !w_gate || !w_up || !w_down || !h_workspace || !y_perm)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x_perm) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) ||
+      !aligned16(h_workspace) || !aligned16(y_perm))
+    return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = as_cuda(stream);
+  if (dtype == MOE_F32) {
+    const int T = 256;
+    const long long n1 = (long long)M_total * F, n2 = (long long)M_total * D;
+    simt::swiglu_up_kernel<<<(unsigned)((n1 + T - 1) / T), T, 0, s>>>(
+        static_cast<const float*>(x_perm), offsets, G, M_total, D, F, static_cast<const float*>(w_gate),
+        static_cast<const float*>(w_up), static_cast<float*>(h_workspace));
+    simt::swiglu_down_kernel<<<(unsigned)((n2 + T - 1) / T), T, 0, s>>>(
+        static_cast<const float*>(h_workspace), offsets, G, M_total, D, F, static_cast<const float*>(w_down),
+        static_cast<float*>(y_perm));
+    return launch_status();
+  }
+  int* status = device_status_word();
+  if (!status) return MOE_ERR_CUDA;
+  CUtensorMap ma, mg, mu, mh, md;
+  if (!tc::make_map(&ma, x_perm, (uint64_t)M_total, (uint64_t)D, tc::BM) ||
+      !tc::make_map(&mg, w_gate, (uint64_t)G * F, (uint64_t)D, tc::BN / 2) ||
+      !tc::make_map(&mu, w_up, (uint64_t)G * F, (uint64_t)D, tc::BN / 2) ||
+      !tc::make_map(&mh, h_workspace, (uint64_t)M_total, (uint64_t)F, tc::BM) ||
+      !tc::make_map(&md, w_down, (uint64_t)G * D, (uint64_t)F, tc::BN))
+    return MOE_ERR_CUDA;
+  moe_status_t st = tc::launch<0>(ma, mg, mu, offsets, G, M_total, D, F, h_workspace, status, s);
+  if (st != MOE_OK) return st;
+  return tc::launch<1>(mh, md, md, offsets, G, M_total, F, D, y_perm, status, s);
+}

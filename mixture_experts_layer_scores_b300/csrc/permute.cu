@@ -1,0 +1,255 @@
+// Per-expert histogram, exclusive scan and stable permutation of routed rows.
+//
+// Lesson "Mixture of Experts", "Build it" step 2 (count how often each expert fires)
+// and the evaluation article's per-expert routed-token histogram.  The permutation
+// lays each expert's tokens out as one contiguous block of rows so the grouped GEMM
+// reads them with TMA; within an expert, rows follow slot order n*k + j (stable).
+//
+// Deterministic, no order-dependent atomics:
+//   1. hist : block b counts the ids of its slot chunk in shared memory -> ws[b][E]
+//   2. scan : one block turns ws into per-block bases (offsets[e] + rows of expert e
+//             in earlier chunks) and writes counts / offsets
+//   3. rank : block b walks its chunk in slot order; __match_any_sync gives each slot
+//             its rank among same-expert slots of the warp, a per-warp table orders the
+//             warps; row = base + rank.  Writes row_map and perm_token.
+//   4. copy : grid-stride 16-byte row moves xn[n] -> x_perm[row_map[n, j]], each source
+//             vector read once and written k times.
+#include "moe_internal.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kChunkBlocks = 128;  // target number of slot chunks
+
+struct Plan {
+  int tpb;  // tokens per chunk
+  int nb;   // number of chunks
+};
+
+Plan plan(int N) {
+  Plan p;
+  p.tpb = (N + kChunkBlocks - 1) / kChunkBlocks;
+  if (p.tpb < 1) p.tpb = 1;
+  p.nb = (N + p.tpb - 1) / p.tpb;
+  return p;
+}
+
+__global__ void __launch_bounds__(256) hist_kernel(const int32_t* __restrict__ idx, int R, int E,
+                                                   int C, int32_t* __restrict__ ws,
+                                                   int* __restrict__ status) {
+  extern __shared__ int sh[];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) sh[e] = 0;
+  __syncthreads();
+  const int s0 = blockIdx.x * C, s1 = min(R, s0 + C);
+  bool bad = false;
+  for (int s = s0 + threadIdx.x; s < s1; s += blockDim.x) {
+    const int e = idx[s];
+    if (e >= 0 && e < E) atomicAdd(&sh[e], 1);
+    else bad = true;
+  }
+  if (bad) atomicOr(status, kStatusBadExpertId);
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) ws[(size_t)blockIdx.x * E + e] = sh[e];
+}
+
+// One block of 1024 threads, E <= 1024.  Thread (g, e) owns expert e over chunk range g.
+__global__ void __launch_bounds__(1024) scan_kernel(int32_t* __restrict__ ws, int nb, int E,
+                                                    int32_t* __restrict__ counts,
+                                                    int32_t* __restrict__ offsets) {
+  extern __shared__ int sh[];  // part[P][E], cnt[E], wsum[32]
+  const int P = blockDim.x / E;
+  int* part = sh;
+  int* cnt = sh + P * E;
+  int* wsum = cnt + E;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int g = t / E, e = t % E;
+  const int per = (nb + P - 1) / P;
+  const int b0 = g * per, b1 = min(nb, b0 + per);
+  if (g < P) {
+    int sum = 0;
+    for (int b = b0; b < b1; ++b) sum += ws[(size_t)b * E + e];
+    part[g * E + e] = sum;
+  }
+  __syncthreads();
+  if (t < E) {  // exclusive prefix over chunk groups, per expert
+    int c = 0;
+    for (int gg = 0; gg < P; ++gg) {
+      const int v = part[gg * E + t];
+      part[gg * E + t] = c;
+      c += v;
+    }
+    cnt[t] = c;
+  }
+  __syncthreads();
+  // block-wide exclusive scan of cnt[0..E)
+  const int mine = t < E ? cnt[t] : 0;
+  int v = mine;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, v, off);
+    if (lane >= off) v += y;
+  }
+  if (lane == 31) wsum[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    int w = wsum[lane];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, off);
+      if (lane >= off) w += y;
+    }
+    wsum[lane] = w;
+  }
+  __syncthreads();
+  const int excl = v - mine + (warp > 0 ? wsum[warp - 1] : 0);
+  if (t < E) {
+    counts[t] = mine;
+    offsets[t] = excl;
+    if (t == E - 1) offsets[E] = excl + mine;
+  }
+  __syncthreads();
+  if (t < E) cnt[t] = excl;  // reuse as the expert's first row
+  __syncthreads();
+  if (g < P) {
+    int base = cnt[e] + part[g * E + e];
+    for (int b = b0; b < b1; ++b) {
+      const int x = ws[(size_t)b * E + e];
+      ws[(size_t)b * E + e] = base;
+      base += x;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256) rank_kernel(const int32_t* __restrict__ idx, int R, int k,
+                                                   int E, int C, const int32_t* __restrict__ ws,
+                                                   int32_t* __restrict__ row_map,
+                                                   int32_t* __restrict__ perm_token) {
+  extern __shared__ int sh[];
+  int* running = sh;          // [E]
+  int* wcnt = sh + E;         // [8][E]
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  for (int e = t; e < E; e += 256) {
+    running[e] = ws[(size_t)blockIdx.x * E + e];
+#pragma unroll
+    for (int w = 0; w < 8; ++w) wcnt[w * E + e] = 0;
+  }
+  __syncthreads();
+  const int s0 = blockIdx.x * C, s1 = min(R, s0 + C);
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int base = s0; base < s1; base += 256) {
+    const int s = base + t;
+    int e = -1;
+    if (s < s1) {
+      e = idx[s];
+      if (e < 0 || e >= E) e = -1;
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & lt_mask);
+    if (e >= 0 && rank == 0) wcnt[warp * E + e] = __popc(peers);
+    __syncthreads();
+    if (e >= 0) {
+      int pre = 0;
+      for (int w = 0; w < warp; ++w) pre += wcnt[w * E + e];
+      const int row = running[e] + pre + rank;
+      row_map[s] = row;
+      perm_token[row] = s / k;
+    } else if (s < s1) {
+      row_map[s] = -1;
+    }
+    __syncthreads();
+    for (int x = t; x < E; x += 256) {
+      int sum = 0;
+#pragma unroll
+      for (int w = 0; w < 8; ++w) {
+        sum += wcnt[w * E + x];
+        wcnt[w * E + x] = 0;
+      }
+      running[x] += sum;
+    }
+    __syncthreads();
+  }
+}
+
+// x_perm[row_map[n, j]] = xn[n] in 16-byte vectors; V vectors per row.
+__global__ void __launch_bounds__(256) copy_kernel(const uint4* __restrict__ xn, int N, int V, int k,
+                                                   const int32_t* __restrict__ row_map,
+                                                   uint4* __restrict__ x_perm) {
+  constexpr int U = 4;
+  const long long total = (long long)N * V;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i0 = (long long)blockIdx.x * blockDim.x + threadIdx.x; i0 < total; i0 += stride * U) {
+    uint4 v[U];
+    long long it[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      it[u] = i0 + u * stride;
+      if (it[u] < total) v[u] = __ldg(xn + it[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (it[u] >= total) continue;
+      const int n = (int)(it[u] / V), c = (int)(it[u] % V);
+      for (int j = 0; j < k; ++j) {
+        const int row = __ldg(row_map + (size_t)n * k + j);
+        if (row >= 0) x_perm[(size_t)row * V + c] = v[u];
+      }
+    }
+  }
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" size_t moe_permute_workspace_bytes(int N, int k, int E) {
+  if (N <= 0 || k <= 0 || E <= 0) return 0;
+  const moe::Plan p = moe::plan(N);
+  return (size_t)p.nb * (size_t)E * sizeof(int32_t);
+}
+
+extern "C" moe_status_t moe_permute(const void* xn, moe_dtype_t dtype, int N, int D,
+                                    const int32_t* topk_idx, int k, int E, int32_t* counts,
+                                    int32_t* offsets, int32_t* row_map, int32_t* perm_token,
+                                    void* x_perm, void* workspace, size_t workspace_bytes,
+                                    moe_stream_t stream) {
+  using namespace moe;
+  if (N < 0 || k < 1 || E < 1 || k > E || D <= 0) return MOE_ERR_INVALID_ARG;
+  if (E > 1024 || (long long)N * k >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
+  if (dtype != MOE_BF16 && dtype != MOE_F32) return MOE_ERR_UNSUPPORTED;
+  if (!counts || !offsets) return MOE_ERR_INVALID_ARG;
+  if ((row_map == nullptr) != (perm_token == nullptr)) return MOE_ERR_INVALID_ARG;
+  if (x_perm && (!row_map || !xn)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = as_cuda(stream);
+  if (N == 0) {
+    if (cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (E + 1), s) != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_OK;
+  }
+  if (!topk_idx || !workspace) return MOE_ERR_INVALID_ARG;
+  if (workspace_bytes < moe_permute_workspace_bytes(N, k, E)) return MOE_ERR_INVALID_ARG;
+  const size_t esize = dtype == MOE_BF16 ? 2 : 4;
+  if (x_perm && ((D * esize) % 16 != 0 || !aligned16(xn) || !aligned16(x_perm)))
+    return MOE_ERR_INVALID_ARG;
+  int* status = device_status_word();
+  if (!status) return MOE_ERR_CUDA;
+
+  const Plan p = plan(N);
+  const int R = N * k, C = p.tpb * k;
+  int32_t* ws = static_cast<int32_t*>(workspace);
+  hist_kernel<<<p.nb, 256, E * sizeof(int), s>>>(topk_idx, R, E, C, ws, status);
+  const int P = 1024 / E;
+  scan_kernel<<<1, 1024, (size_t)(P * E + E + 32) * sizeof(int), s>>>(ws, p.nb, E, counts, offsets);
+  if (row_map) {
+    rank_kernel<<<p.nb, 256, (size_t)9 * E * sizeof(int), s>>>(topk_idx, R, k, E, C, ws, row_map,
+                                                                perm_token);
+  }
+  if (x_perm) {
+    const int V = (int)(D * esize / 16);
+    long long items = (long long)N * V;
+    long long blocks = (items + 256 * 4 - 1) / (256 * 4);
+    const long long cap = (long long)sm_count() * 8;
+    if (blocks > cap) blocks = cap;
+    copy_kernel<<<(int)blocks, 256, 0, s>>>(static_cast<const uint4*>(xn), N, V, k, row_map,
+                                            static_cast<uint4*>(x_perm));
+  }
+  return launch_status();
+}

@@ -1,0 +1,268 @@
+"""Python binding of the C ABI in include/moe.h (ctypes; argument marshalling only).
+
+Every function takes torch CUDA tensors, passes their device pointers and the current
+torch stream to the library, and raises ``MoEError`` on a non-zero status.  Outputs
+that are not supplied are allocated with ``torch.empty`` on the input's device.
+There is no CPU path: without the built ``libmoe.so`` every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe.so")
+_lib = None
+
+MOE_F32, MOE_BF16 = 0, 1
+SCORE_FN = {"softmax": 0, "sigmoid": 1}
+STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED", -3: "MOE_ERR_CUDA",
+          -4: "MOE_ERR_TIMEOUT", -5: "MOE_ERR_NAN_INPUT"}
+EXPORTS = ("moe_status_string", "moe_last_device_status", "moe_version", "moe_router_topk",
+           "moe_permute_workspace_bytes", "moe_permute", "moe_grouped_swiglu",
+           "moe_unpermute_combine", "moe_bias_update")
+
+
+class MoEError(RuntimeError):
+    def __init__(self, fn, status):
+        super().__init__(f"{fn} returned {STATUS.get(status, status)}")
+        self.status = status
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def load():
+    """Load libmoe.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError(f"CUDA library not built: {_LIB_PATH} (run __graft_entry__.build())")
+    L = ctypes.CDLL(_LIB_PATH)
+    vp, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    sig = {
+        "moe_status_string": ([i32], ctypes.c_char_p),
+        "moe_last_device_status": ([vp], i32),
+        "moe_version": ([], i32),
+        "moe_router_topk": ([vp, i32, i32, i32, vp, vp, i32, i32, i32, vp, vp, vp, vp, vp], i32),
+        "moe_permute_workspace_bytes": ([i32, i32, i32], sz),
+        "moe_permute": ([vp, i32, i32, i32, vp, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp], i32),
+        "moe_grouped_swiglu": ([vp, i32, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp], i32),
+        "moe_unpermute_combine": ([vp, vp, vp, i32, i32, i32, vp, vp, vp, i32, vp], i32),
+        "moe_bias_update": ([vp, i32, i64, f32, vp, vp, vp], i32),
+    }
+    for name, (args, res) in sig.items():
+        f = getattr(L, name)
+        f.argtypes, f.restype = args, res
+    _lib = L
+    return L
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dt(t):
+    if t.dtype == torch.bfloat16:
+        return MOE_BF16
+    if t.dtype == torch.float32:
+        return MOE_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _chk(name, st):
+    if st != 0:
+        raise MoEError(name, st)
+
+
+def _cuda(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("tensors must be contiguous CUDA tensors")
+
+
+def last_device_status(stream=None) -> int:
+    return load().moe_last_device_status(_stream(stream))
+
+
+def version() -> int:
+    return load().moe_version()
+
+
+def moe_router_topk(xn, w_router, bias, k, score_fn="softmax", logits_out=None, topk_idx=None,
+                    topk_gate=None, near_tie=None, want_logits=True, want_near_tie=True, stream=None):
+    """Router GEMM + biased top-k + gates.  Returns (logits, idx, gate, near_tie)."""
+    L = load()
+    N, D = xn.shape
+    E = w_router.shape[0]
+    dev = xn.device
+    if logits_out is None and want_logits:
+        logits_out = torch.empty(N, E, dtype=torch.float32, device=dev)
+    if topk_idx is None:
+        topk_idx = torch.empty(N, k, dtype=torch.int32, device=dev)
+    if topk_gate is None:
+        topk_gate = torch.empty(N, k, dtype=torch.float32, device=dev)
+    if near_tie is None and want_near_tie:
+        near_tie = torch.empty(N, dtype=torch.uint8, device=dev)
+    _cuda(xn, w_router, bias, logits_out, topk_idx, topk_gate, near_tie)
+    _chk("moe_router_topk", L.moe_router_topk(
+        _p(xn), _dt(xn), N, D, _p(w_router), _p(bias), E, k, SCORE_FN[score_fn], _p(logits_out),
+        _p(topk_idx), _p(topk_gate), _p(near_tie), _stream(stream)))
+    return logits_out, topk_idx, topk_gate, near_tie
+
+
+def permute_workspace_bytes(N, k, E) -> int:
+    return int(load().moe_permute_workspace_bytes(N, k, E))
+
+
+def moe_permute(xn, topk_idx, E, counts=None, offsets=None, row_map=None, perm_token=None,
+                x_perm=None, workspace=None, rows=True, copy=True, stream=None):
+    """Histogram + scan + stable permutation.  Returns (counts, offsets, row_map, perm_token, x_perm)."""
+    L = load()
+    N, k = topk_idx.shape
+    dev = topk_idx.device
+    D = xn.shape[1] if xn is not None else 64
+    if counts is None:
+        counts = torch.empty(E, dtype=torch.int32, device=dev)
+    if offsets is None:
+        offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    if rows and row_map is None:
+        row_map = torch.empty(N, k, dtype=torch.int32, device=dev)
+    if rows and perm_token is None:
+        perm_token = torch.empty(N * k, dtype=torch.int32, device=dev)
+    if copy and x_perm is None:
+        x_perm = torch.empty(N * k, D, dtype=xn.dtype, device=dev)
+    if workspace is None:
+        workspace = torch.empty(max(1, permute_workspace_bytes(N, k, E)), dtype=torch.uint8, device=dev)
+    dt = _dt(xn) if xn is not None else MOE_BF16
+    _cuda(xn, topk_idx, counts, offsets, row_map, perm_token, x_perm, workspace)
+    _chk("moe_permute", L.moe_permute(
+        _p(xn) if copy else None, dt, N, D, _p(topk_idx), k, E, _p(counts), _p(offsets),
+        _p(row_map), _p(perm_token), _p(x_perm) if copy else None, _p(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return counts, offsets, row_map, perm_token, x_perm
+
+
+def moe_grouped_swiglu(x_perm, offsets, w_gate, w_up, w_down, h_workspace=None, y_perm=None,
+                       stream=None):
+    """Grouped SwiGLU over per-group row blocks.  Returns y_perm."""
+    L = load()
+    M, D = x_perm.shape
+    G, F, _ = w_gate.shape
+    if h_workspace is None:
+        h_workspace = torch.empty(M, F, dtype=x_perm.dtype, device=x_perm.device)
+    if y_perm is None:
+        y_perm = torch.empty(M, D, dtype=x_perm.dtype, device=x_perm.device)
+    _cuda(x_perm, offsets, w_gate, w_up, w_down, h_workspace, y_perm)
+    _chk("moe_grouped_swiglu", L.moe_grouped_swiglu(
+        _p(x_perm), _dt(x_perm), _p(offsets), G, M, D, F, _p(w_gate), _p(w_up), _p(w_down),
+        _p(h_workspace), _p(y_perm), _stream(stream)))
+    return y_perm
+
+
+def moe_unpermute_combine(y_perm, row_map, topk_gate, shared_y=None, residual=None, out=None,
+                          stream=None):
+    """out = residual + shared_y + sum_j gate[:, j] * y_perm[row_map[:, j]]."""
+    L = load()
+    N, k = row_map.shape
+    D = y_perm.shape[1]
+    if out is None:
+        out = torch.empty(N, D, dtype=y_perm.dtype, device=y_perm.device)
+    _cuda(y_perm, row_map, topk_gate, shared_y, residual, out)
+    _chk("moe_unpermute_combine", L.moe_unpermute_combine(
+        _p(y_perm), _p(row_map), _p(topk_gate), N, k, D, _p(shared_y), _p(residual), _p(out),
+        _dt(y_perm), _stream(stream)))
+    return out
+
+
+def moe_bias_update(counts, bias, total_assignments, gamma, max_over_mean=None, stream=None):
+    """bias += gamma * sign(total/E - counts), in place.  Returns max_over_mean (device fp32[1])."""
+    L = load()
+    E = counts.shape[0]
+    if max_over_mean is None:
+        max_over_mean = torch.empty(1, dtype=torch.float32, device=counts.device)
+    _cuda(counts, bias, max_over_mean)
+    _chk("moe_bias_update", L.moe_bias_update(
+        _p(counts), E, int(total_assignments), float(gamma), _p(bias), _p(max_over_mean),
+        _stream(stream)))
+    return max_over_mean
+
+
+# ----------------------------------------------------------------------------------------
+# The whole layer: buffers allocated once, then the five calls in order.
+# ----------------------------------------------------------------------------------------
+
+@dataclass
+class LayerWeights:
+    w_router: torch.Tensor               # [E, D] fp32
+    bias: torch.Tensor                   # [E] fp32 (updated in place by the bias step)
+    w_gate: torch.Tensor                 # [E, F, D]
+    w_up: torch.Tensor                   # [E, F, D]
+    w_down: torch.Tensor                 # [E, D, F]
+    shared: tuple | None = None          # (w_gate[1,Fs,D], w_up[1,Fs,D], w_down[1,D,Fs]) or None
+
+
+class MoELayer:
+    """Top-k MoE FFN layer forward on one GPU, with reusable device buffers."""
+
+    def __init__(self, weights: LayerWeights, N: int, k: int, score_fn="softmax", gamma=1e-3,
+                 dtype=torch.bfloat16):
+        w = weights
+        self.w, self.k, self.score_fn, self.gamma = w, k, score_fn, gamma
+        self.N = N
+        self.E, self.D = w.w_router.shape
+        self.F = w.w_gate.shape[1]
+        dev = w.w_router.device
+        R = N * k
+        e = lambda *s, dt=torch.int32: torch.empty(*s, dtype=dt, device=dev)
+        self.logits = e(N, self.E, dt=torch.float32)
+        self.idx = e(N, k)
+        self.gate = e(N, k, dt=torch.float32)
+        self.near_tie = e(N, dt=torch.uint8)
+        self.counts = e(self.E)
+        self.offsets = e(self.E + 1)
+        self.row_map = e(N, k)
+        self.perm_token = e(R)
+        self.x_perm = e(R, self.D, dt=dtype)
+        self.h_ws = e(R, self.F, dt=dtype)
+        self.y_perm = e(R, self.D, dt=dtype)
+        self.out = e(N, self.D, dt=dtype)
+        self.workspace = e(max(1, permute_workspace_bytes(N, k, self.E)), dt=torch.uint8)
+        self.mom = e(1, dt=torch.float32)
+        if w.shared is not None:
+            Fs = w.shared[0].shape[1]
+            self.sh_offsets = torch.tensor([0, N], dtype=torch.int32, device=dev)
+            self.sh_h = e(N, Fs, dt=dtype)
+            self.sh_y = e(N, self.D, dt=dtype)
+        else:
+            self.sh_y = None
+
+    def forward(self, xn, h, update_bias=True, stream=None):
+        """out = h + shared(xn) + sum_j gate_j Expert_j(xn); then the +-gamma bias step."""
+        w = self.w
+        moe_router_topk(xn, w.w_router, w.bias, self.k, self.score_fn, self.logits, self.idx,
+                        self.gate, self.near_tie, stream=stream)
+        moe_permute(xn, self.idx, self.E, self.counts, self.offsets, self.row_map,
+                    self.perm_token, self.x_perm, self.workspace, stream=stream)
+        moe_grouped_swiglu(self.x_perm, self.offsets, w.w_gate, w.w_up, w.w_down, self.h_ws,
+                           self.y_perm, stream=stream)
+        if w.shared is not None:
+            moe_grouped_swiglu(xn, self.sh_offsets, w.shared[0], w.shared[1], w.shared[2],
+                               self.sh_h, self.sh_y, stream=stream)
+        moe_unpermute_combine(self.y_perm, self.row_map, self.gate, self.sh_y, h, self.out,
+                              stream=stream)
+        if update_bias:
+            moe_bias_update(self.counts, w.bias, self.N * self.k, self.gamma, self.mom,
+                            stream=stream)
+        return self.out
+
+    kernels_per_forward = property(lambda self: 1 + 4 + 2 + (2 if self.w.shared else 0) + 1 + 1)

@@ -1,0 +1,84 @@
+"""The C-ABI library builds for sm_103a, loads without a GPU and exports every symbol the
+header declares; host-side argument checks reject bad calls before any launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from mixture_experts_layer_scores_b300 import build, moe
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = []
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if h.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", h)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"\b(moe_[a-z_0-9]+)\s*\(", src)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return moe.load()
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for fn in ("moe_router_topk", "moe_permute", "moe_grouped_swiglu", "moe_unpermute_combine",
+               "moe_bias_update"):
+        assert fn in names
+
+
+def test_every_declared_symbol_exported(lib):
+    raw = ctypes.CDLL(moe.lib_path())
+    for name in declared_functions():
+        assert hasattr(raw, name), name
+    assert set(moe.EXPORTS) <= set(declared_functions())
+
+
+def test_status_strings(lib):
+    for code, name in moe.STATUS.items():
+        assert lib.moe_status_string(code).decode() == name
+    assert lib.moe_version() >= 100
+
+
+def test_workspace_size(lib):
+    assert lib.moe_permute_workspace_bytes(0, 8, 64) == 0
+    b = lib.moe_permute_workspace_bytes(8192, 8, 64)
+    assert b > 0 and b % 4 == 0 and b <= 128 * 64 * 4
+
+
+def test_host_validation_rejects_before_launch(lib):
+    vp = ctypes.c_void_p
+    # k > E, E too large, D not a multiple of 64, null outputs: no launch happens
+    assert lib.moe_router_topk(vp(16), 1, 4, 64, vp(16), None, 4, 5, 0, None, vp(16), vp(16), None, None) == -1
+    assert lib.moe_router_topk(vp(16), 1, 4, 64, vp(16), None, 300, 5, 0, None, vp(16), vp(16), None, None) == -2
+    assert lib.moe_router_topk(vp(16), 1, 4, 48, vp(16), None, 8, 2, 0, None, vp(16), vp(16), None, None) == -2
+    assert lib.moe_router_topk(vp(16), 1, 4, 64, vp(16), None, 8, 2, 0, None, None, vp(16), None, None) == -1
+    assert lib.moe_router_topk(vp(16), 1, 4, 64, vp(16), None, 8, 2, 7, None, vp(16), vp(16), None, None) == -1
+    # unaligned activation pointer
+    assert lib.moe_router_topk(vp(18), 1, 4, 64, vp(16), None, 8, 2, 0, None, vp(16), vp(16), None, None) == -1
+    # permute: workspace too small, row_map without perm_token
+    assert lib.moe_permute(vp(16), 1, 64, 64, vp(16), 2, 8, vp(16), vp(16), vp(16), vp(16), vp(16),
+                           vp(16), 4, None) == -1
+    assert lib.moe_permute(vp(16), 1, 64, 64, vp(16), 2, 8, vp(16), vp(16), vp(16), None, None,
+                           vp(16), 1 << 20, None) == -1
+    # grouped GEMM: F not a multiple of 64; M_total == 0 is a no-op
+    assert lib.moe_grouped_swiglu(vp(16), 1, vp(16), 4, 100, 128, 96, vp(16), vp(16), vp(16), vp(16),
+                                  vp(16), None) == -2
+    assert lib.moe_grouped_swiglu(None, 1, None, 4, 0, 128, 128, None, None, None, None, None, None) == 0
+    # combine: k too large; bias: null counts
+    assert lib.moe_unpermute_combine(vp(16), vp(16), vp(16), 4, 17, 64, None, None, vp(16), 1, None) == -2
+    assert lib.moe_bias_update(None, 8, 64, ctypes.c_float(1e-3), vp(16), None, None) == -1
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(moe, "_lib", None)
+    monkeypatch.setattr(moe, "_LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        moe.load()
