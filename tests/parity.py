@@ -8,7 +8,8 @@ Tolerances (written here, used by every parity test):
   gap below 1e-6 are reported, not failed;
 * counts, offsets, permutation, permuted rows, bias update: bit-exact;
 * bf16 experts with fp32 accumulation (y_perm, out, and the MoE delta out - h):
-  relative Frobenius <= 1e-2 and max abs <= 3e-2 * rms(reference);
+  relative Frobenius <= 1e-2 and max abs <= 3e-2 * rms(reference); for the delta the
+  max-abs bound adds half an ulp of |out|, the rounding of the bf16 output itself;
 * fp32 experts (all-fp32 layer): relative Frobenius <= 1e-5 and max abs <= 1e-4 * rms
   (fp32 dot products of a few hundred terms carry ~1e-6 relative error).
 """
@@ -170,5 +171,21 @@ def compare_layer(cfg, g, o, k=None, f32=False):
 
 
 def moe_delta_close(cfg, g, o, h, f32=False):
-    """Tolerance on the MoE delta out - h as well (the residual must not hide errors)."""
-    return assert_close("out - h", np64(g["out"]) - h, o["out"] - h, f32)
+    """Tolerance on the MoE delta out - h as well (the residual must not hide errors).
+
+    The GPU's out is rounded once to the output dtype, so each element of out - h also
+    carries up to half an ulp of |out| on top of the expert error; the max-abs bound is
+    3e-2 * rms(delta) plus that half ulp (relative Frobenius stays 1e-2)."""
+    got = np64(g["out"]) - h
+    ref = o["out"] - h
+    rf, mr = (F32_REL_FRO, F32_MAX_RMS) if f32 else (BF16_REL_FRO, BF16_MAX_RMS)
+    a = rel_fro(got, ref)
+    assert a <= rf, f"out - h: rel_fro={a:.3e} (<= {rf})"
+    mant_bits = 24 if f32 else 8
+    _, ex = np.frexp(np.abs(o["out"]))
+    half_ulp = np.ldexp(1.0, ex - mant_bits - 1)
+    rms = float(np.sqrt(np.mean(ref ** 2)))
+    excess = np.abs(got - ref) - half_ulp
+    b = float(np.max(excess) / rms)
+    assert b <= mr, f"out - h: (max abs - half ulp of out)/rms = {b:.3e} (<= {mr})"
+    return a, b
