@@ -122,6 +122,31 @@ moe_status_t moe_permute(const void* xn, moe_dtype_t dtype, int N, int D,
                          moe_stream_t stream);
 
 /*
+ * moe_permute_noalloc -- moe_permute without a caller-supplied workspace.
+ * The pages have no counterpart to this call; it exists for callers that cannot
+ * allocate device memory at all: a plugin handed only its input and output buffers
+ * by a host framework that owns every device allocation, or code that must not take
+ * the cost and device-wide synchronisation of cudaMalloc/cudaFree on its path.
+ *
+ * Arguments and results are those of moe_permute.  Its scratch (the per-chunk expert
+ * histograms) lives in a fixed array inside the library, of
+ * moe_permute_noalloc_max_scratch_bytes() bytes (256 KiB), which every GPU that loads
+ * the library holds until the process exits.  A size needing more scratch than that
+ * (moe_permute_workspace_bytes(N, k, E) larger than the array) is rejected with
+ * MOE_ERR_UNSUPPORTED before anything is launched.  No call allocates or frees memory.
+ * The first call on a device looks up the array's device address once for that device
+ * (a CUDA runtime query); make that first call before any stream capture.  All calls on
+ * a device share the one array and nothing in it needs to start at zero; calls that
+ * overlap on the GPU (on different streams without ordering) race on it and must not
+ * be issued.
+ */
+size_t moe_permute_noalloc_max_scratch_bytes(void);
+moe_status_t moe_permute_noalloc(const void* xn, moe_dtype_t dtype, int N, int D,
+                                 const int32_t* topk_idx, int k, int E, int32_t* counts,
+                                 int32_t* offsets, int32_t* row_map, int32_t* perm_token,
+                                 void* x_perm, moe_stream_t stream);
+
+/*
  * moe_grouped_swiglu -- every expert's SwiGLU FFN on its block of permuted rows.
  * Lesson "Concept" (each expert an independent SwiGLU FFN) and "Shared experts"
  * (call with G = 1 and offsets = {0, N} on xn for the always-on expert).

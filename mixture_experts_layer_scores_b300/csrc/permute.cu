@@ -253,3 +253,50 @@ extern "C" moe_status_t moe_permute(const void* xn, moe_dtype_t dtype, int N, in
   }
   return launch_status();
 }
+
+// ---- moe_permute_noalloc ---------------------------------------------------------------
+// The same permutation for callers that cannot allocate device memory: its scratch lives
+// in a fixed file-scope device array that every GPU loading the library holds until exit.
+#include <mutex>
+
+namespace moe {
+namespace {
+
+constexpr size_t kNoAllocScratchInts = 65536;  // 256 KiB
+static __device__ __align__(256) int32_t g_permute_scratch[kNoAllocScratchInts];
+
+// Device address of g_permute_scratch on the current device, looked up once per device.
+int32_t* noalloc_scratch() {
+  static std::mutex mu;
+  static int32_t* addr[128] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    int32_t* p = nullptr;
+    if (cudaGetSymbolAddress((void**)&p, g_permute_scratch) != cudaSuccess) return nullptr;
+    addr[dev] = p;
+  }
+  return addr[dev];
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" size_t moe_permute_noalloc_max_scratch_bytes(void) {
+  return moe::kNoAllocScratchInts * sizeof(int32_t);
+}
+
+extern "C" moe_status_t moe_permute_noalloc(const void* xn, moe_dtype_t dtype, int N, int D,
+                                            const int32_t* topk_idx, int k, int E, int32_t* counts,
+                                            int32_t* offsets, int32_t* row_map, int32_t* perm_token,
+                                            void* x_perm, moe_stream_t stream) {
+  using namespace moe;
+  if (N < 0 || k < 1 || E < 1 || k > E || D <= 0) return MOE_ERR_INVALID_ARG;
+  const size_t need = moe_permute_workspace_bytes(N, k, E);
+  if (need > kNoAllocScratchInts * sizeof(int32_t)) return MOE_ERR_UNSUPPORTED;
+  int32_t* scratch = noalloc_scratch();
+  if (!scratch) return MOE_ERR_CUDA;
+  return moe_permute(xn, dtype, N, D, topk_idx, k, E, counts, offsets, row_map, perm_token, x_perm,
+                     scratch, kNoAllocScratchInts * sizeof(int32_t), stream);
+}

@@ -22,7 +22,8 @@ STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED", -3:
           -4: "MOE_ERR_TIMEOUT", -5: "MOE_ERR_NAN_INPUT"}
 EXPORTS = ("moe_status_string", "moe_last_device_status", "moe_version", "moe_router_topk",
            "moe_permute_workspace_bytes", "moe_permute", "moe_grouped_swiglu",
-           "moe_unpermute_combine", "moe_bias_update")
+           "moe_unpermute_combine", "moe_bias_update", "moe_permute_noalloc",
+           "moe_permute_noalloc_max_scratch_bytes")
 
 
 class MoEError(RuntimeError):
@@ -54,6 +55,8 @@ def load():
         "moe_grouped_swiglu": ([vp, i32, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp], i32),
         "moe_unpermute_combine": ([vp, vp, vp, i32, i32, i32, vp, vp, vp, i32, vp], i32),
         "moe_bias_update": ([vp, i32, i64, f32, vp, vp, vp], i32),
+        "moe_permute_noalloc": ([vp, i32, i32, i32, vp, i32, i32, vp, vp, vp, vp, vp, vp], i32),
+        "moe_permute_noalloc_max_scratch_bytes": ([], sz),
     }
     for name, (args, res) in sig.items():
         f = getattr(L, name)
@@ -149,6 +152,22 @@ def moe_permute(xn, topk_idx, E, counts=None, offsets=None, row_map=None, perm_t
         _p(xn) if copy else None, dt, N, D, _p(topk_idx), k, E, _p(counts), _p(offsets),
         _p(row_map), _p(perm_token), _p(x_perm) if copy else None, _p(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
+    return counts, offsets, row_map, perm_token, x_perm
+
+
+def moe_permute_noalloc(xn, topk_idx, E, counts, offsets, row_map, perm_token, x_perm,
+                        stream=None):
+    """moe_permute for callers that cannot allocate device memory: the library keeps the
+    scratch in a fixed array of its own, so only inputs and outputs are passed in (all of
+    them must already exist).  Calls on one device share that array: never run two at
+    once on unordered streams."""
+    L = load()
+    N, k = topk_idx.shape
+    D = xn.shape[1]
+    _cuda(xn, topk_idx, counts, offsets, row_map, perm_token, x_perm)
+    _chk("moe_permute_noalloc", L.moe_permute_noalloc(
+        _p(xn), _dt(xn), N, D, _p(topk_idx), k, E, _p(counts), _p(offsets), _p(row_map),
+        _p(perm_token), _p(x_perm), _stream(stream)))
     return counts, offsets, row_map, perm_token, x_perm
 
 
