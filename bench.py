@@ -153,8 +153,7 @@ class Step:
         h = self.h if h is None else h
         rec = (lambda i: events[i].record()) if events is not None else (lambda i: None)
         rec(0)
-        moe.moe_router_topk(xn, w.w_router, w.bias, L.k, L.score_fn, L.logits, L.idx, L.gate,
-                            L.near_tie)
+        L.route(xn)
         rec(1)
         moe.moe_permute(xn, L.idx, L.E, L.counts, L.offsets, L.row_map, L.perm_token, L.x_perm,
                         L.workspace)

@@ -94,6 +94,39 @@ moe_status_t moe_router_topk(const void* xn, moe_dtype_t x_dtype, int N, int D,
                              moe_score_fn_t fn, float* logits_out, int32_t* topk_idx,
                              float* topk_gate, uint8_t* near_tie, moe_stream_t stream);
 
+/* Bytes of the split router weight moe_router_split writes: 3 * E * D bf16. */
+size_t moe_router_split_bytes(int E, int D);
+
+/*
+ * moe_router_split -- write the fp32 router weight as three bf16 planes.
+ * w_split [3, E, D] bf16 (plane 0 = hi, 1 = mid, 2 = lo) with w = hi + mid + lo exactly
+ * for every finite w of magnitude above 2^-110 (each plane keeps the next 8 significant
+ * bits).  Run once per change of w_router; moe_router_topk_split reads the planes.
+ */
+moe_status_t moe_router_split(const float* w_router, int E, int D, void* w_split, moe_stream_t stream);
+
+/*
+ * moe_router_topk_split -- moe_router_topk on tensor cores, for bf16 activations.
+ * Same router as moe_router_topk (lesson "Build it" step 1; the handbook article's fp32
+ * router): logits = xn . (hi + mid + lo)^T, every bf16 x bf16 product exact.  The hi plane
+ * is summed per 64-element slice of D in a fresh fp32 TMEM accumulator and the slice
+ * partials are added in fp32 with two-sum compensation; the mid and lo planes (2^-8 and
+ * 2^-16 of the weight) accumulate over all of D on the tensor cores.  Short batches split
+ * D across CTAs; their partial logits go to `workspace` and are added in split order.
+ *   xn        [N, D] bf16
+ *   w_split   [3, E, D] bf16 from moe_router_split
+ *   logits_out[N, E] fp32 -- REQUIRED here (the top-k reads it back)
+ *   workspace moe_router_topk_split_workspace_bytes(N, D, E) bytes (may be 0 / NULL)
+ *   bias, topk_idx, topk_gate, near_tie, fn, k: as moe_router_topk.
+ * Requires 1 <= k <= min(E, 16), 1 <= E <= 256, D % 64 == 0.
+ */
+size_t moe_router_topk_split_workspace_bytes(int N, int D, int E);
+moe_status_t moe_router_topk_split(const void* xn, int N, int D, const void* w_split,
+                                   const float* bias, int E, int k, moe_score_fn_t fn,
+                                   float* logits_out, int32_t* topk_idx, float* topk_gate,
+                                   uint8_t* near_tie, void* workspace, size_t workspace_bytes,
+                                   moe_stream_t stream);
+
 /* Bytes of scratch moe_permute needs for (N, k, E). */
 size_t moe_permute_workspace_bytes(int N, int k, int E);
 

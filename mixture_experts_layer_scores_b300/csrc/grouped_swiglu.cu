@@ -24,13 +24,10 @@
 // its TMEM and returns.
 //
 // fp32 path: plain CUDA-core kernels (one thread per output element).
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
 #include <algorithm>
 #include <mutex>
 
-#include "moe_internal.cuh"
+#include "tc_common.cuh"
 
 namespace moe {
 namespace tc {
@@ -46,123 +43,11 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int THREADS = 192;
 constexpr int TMEM_COLS = 512;
 constexpr int MAX_GROUPS = 1024;
-constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;  // 2 s
 
-// kind::f16 instruction descriptor: D = f32, A = B = bf16, both K-major, N = 256, M = 128.
-constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
-                           ((uint32_t)(BM >> 4) << 24);
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ unsigned long long now_ns() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Bounded wait.  Returns false if the kernel is aborting (honour_abort) or the wait
-// exceeded WAIT_LIMIT_NS, in which case it raises the abort flag and the status word.
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                       int* status, bool honour_abort) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = now_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0) {
-      if (honour_abort && *abort_flag) return false;
-      if (now_ns() - t0 > WAIT_LIMIT_NS) {
-        *abort_flag = 1;
-        atomicOr(status, kStatusTimeout);
-        return false;
-      }
-    }
-  }
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                            uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-      : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);  // start address
-  d |= (uint64_t)1 << 16;                    // leading byte offset (unused with swizzle)
-  d |= (uint64_t)(1024 >> 4) << 32;          // stride byte offset
-  d |= (uint64_t)1 << 46;                    // descriptor version
-  d |= (uint64_t)2 << 61;                    // 128-byte swizzle
-  return d;
-}
-
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accum) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(IDESC), "r"(accum)
-      : "memory");
-}
-
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-               : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
-        "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
-        "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-}
-
-__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+constexpr uint32_t IDESC = idesc_bf16(BM, BN);
 
 struct Tile {
-  int g, row0, rows, nb;
+  int g, row0, rows, nb, mb;
 };
 
 __device__ __forceinline__ Tile decode(int tile, const int* tile_start, int G, const int32_t* offsets,
@@ -180,6 +65,7 @@ __device__ __forceinline__ Tile decode(int tile, const int* tile_start, int G, c
   const int local = tile - tile_start[lo];
   t.nb = local / mblk;
   const int mb = local - t.nb * mblk;
+  t.mb = mb;
   t.row0 = s + mb * BM;
   t.rows = min(BM, e - t.row0);
   return t;
@@ -219,7 +105,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), 128);
+      mbar_init(tempty_bar(a), 4);  // one arrival per epilogue warp
     }
     mbar_init(done_bar, 1);
     *abort_flag = 0;
@@ -323,7 +209,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
           const uint32_t b_base = a_base + A_BYTES;
 #pragma unroll
           for (int k = 0; k < BK / UK; ++k)
-            tc_mma(d_tmem, sw128_desc(a_base + k * UK * 2), sw128_desc(b_base + k * UK * 2),
+            tc_mma(d_tmem, sw128_desc(a_base + k * UK * 2), sw128_desc(b_base + k * UK * 2), IDESC,
                    (kb | k) != 0 ? 1u : 0u);
           tc_commit(empty_bar(stage));
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -391,7 +277,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
         }
       }
       tc_fence_before();
-      mbar_arrive(tempty_bar(acc));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty_bar(acc));
       if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
     }
   }
@@ -421,8 +308,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2D bf16 row-major [rows, cols] -> box {64 cols, box_rows}, 128-byte swizzle
-bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+bool make_map_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {cols, rows};
@@ -538,11 +424,11 @@ extern "C" moe_status_t moe_grouped_swiglu(const void* x_perm, moe_dtype_t dtype
   int* status = device_status_word();
   if (!status) return MOE_ERR_CUDA;
   CUtensorMap ma, mg, mu, mh, md;
-  if (!tc::make_map(&ma, x_perm, (uint64_t)M_total, (uint64_t)D, tc::BM) ||
-      !tc::make_map(&mg, w_gate, (uint64_t)G * F, (uint64_t)D, tc::BN / 2) ||
-      !tc::make_map(&mu, w_up, (uint64_t)G * F, (uint64_t)D, tc::BN / 2) ||
-      !tc::make_map(&mh, h_workspace, (uint64_t)M_total, (uint64_t)F, tc::BM) ||
-      !tc::make_map(&md, w_down, (uint64_t)G * D, (uint64_t)F, tc::BN))
+  if (!tc::make_map_bf16(&ma, x_perm, (uint64_t)M_total, (uint64_t)D, tc::BM) ||
+      !tc::make_map_bf16(&mg, w_gate, (uint64_t)G * F, (uint64_t)D, tc::BN / 2) ||
+      !tc::make_map_bf16(&mu, w_up, (uint64_t)G * F, (uint64_t)D, tc::BN / 2) ||
+      !tc::make_map_bf16(&mh, h_workspace, (uint64_t)M_total, (uint64_t)F, tc::BM) ||
+      !tc::make_map_bf16(&md, w_down, (uint64_t)G * D, (uint64_t)F, tc::BN))
     return MOE_ERR_CUDA;
   moe_status_t st = tc::launch<0>(ma, mg, mu, offsets, G, M_total, D, F, h_workspace, status, s);
   if (st != MOE_OK) return st;

@@ -1,0 +1,413 @@
+// Router on tensor cores: fp32 router weights split exactly into three bf16 planes.
+//
+// Lesson "Mixture of Experts", "Build it" step 1 (router scores = dot products of the
+// token with every expert's router row); handbook article, router-precision paragraph
+// (bf16 rounding of close logits can change the winner, so the router must keep fp32
+// accuracy).
+//
+// Every fp32 weight w is written as w = hi + mid + lo with three bf16 numbers (8
+// significant bits each, exact for finite normal weights).  The activations are bf16,
+// so every product x*hi, x*mid, x*lo is exact in fp32 and the tensor core computes
+// sum_d x_d * (hi_d + mid_d + lo_d) with fp32 accumulation.  The tensor core's own
+// accumulation over a long reduction is not correctly rounded (measured on B300: 7e-6 to
+// 2e-5 rms logit error when one accumulator spans all of D), so:
+//   * the hi plane is summed per 64-element slice in a fresh TMEM accumulator and the
+//     epilogue warps add the slice partials with two-sum compensation in registers
+//     (measured 8e-8 rms, about the fp32 rounding of the result);
+//   * the mid and lo planes, stacked as one N = 2*NT operand, accumulate across the whole
+//     reduction in a second accumulator: their error is scaled down by 2^-8.
+// An M=128 MMA costs about the same time for any N up to 256 (measured), so this takes 8
+// MMAs per slice instead of 12.  The hand-off per slice is one mbarrier arrival per
+// epilogue warp and a plain add per column, folded into the compensated total every 8
+// slices.  Short token counts are split along D (split-K) so that about
+// 128 CTAs stream the activations; the top-k kernel adds the split partials in order.
+//
+// Kernels: split (w -> 3 bf16 planes), router GEMM (tcgen05, logits [N, E] fp32), and a
+// warp-per-token top-k over the logits (shared selection code with the CUDA-core path).
+#include <algorithm>
+
+#include "tc_common.cuh"
+#include "topk_common.cuh"
+
+namespace moe {
+namespace rtc {
+
+using namespace moe::tc;
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int UK = 16;
+
+__global__ void split_kernel(const float* __restrict__ w, long long n, __nv_bfloat16* __restrict__ out) {
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
+    const float x = w[i];
+    const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+    const float r1 = x - __bfloat162float(hi);    // exact
+    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+    const float r2 = r1 - __bfloat162float(mid);  // exact, <= 8 significant bits
+    out[i] = hi;
+    out[n + i] = mid;
+    out[2 * n + i] = __float2bfloat16_rn(r2);
+  }
+}
+
+// NBUF slice accumulators in TMEM let the MMA warp run up to NBUF-1 slices ahead of the
+// epilogue; EPI epilogue warps share the columns (two warps per TMEM lane quarter when 8).
+template <int NT>
+struct Cfg {
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = NT * BK * 2;  // one split plane
+  static constexpr int STAGE_BYTES = A_BYTES + 3 * B_BYTES;
+  static constexpr int STAGES = NT >= 64 ? 4 : 6;
+  static constexpr int NBUF = NT >= 64 ? 4 : 8;        // hi-plane slice accumulators
+  static constexpr int L_COL = NBUF * NT;              // mid+lo accumulator (2*NT columns)
+  static constexpr int TMEM_COLS = (NBUF + 2) * NT <= 256 ? ((NBUF + 2) * NT <= 128 ? 128 : 256) : 512;
+  static constexpr int EPI = NT >= 32 ? 8 : 4;         // epilogue warps
+  static constexpr int W = NT / (EPI / 4);             // columns per epilogue thread
+  static constexpr int THREADS = 64 + 32 * EPI;
+  static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES + 512;
+};
+
+// Load W consecutive fp32 TMEM columns (W = 16 or 32) of this warp's lane quarter.
+template <int W>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&v)[W]) {
+  if constexpr (W == 16) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+  } else {
+    uint32_t r[32];
+    tmem_ld32(taddr, r);
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+  }
+}
+
+// grid (ceil(N/128), ceil(E/NT)); block = TMA warp, MMA warp, EPI epilogue warps.
+template <int NT>
+__global__ void __launch_bounds__(Cfg<NT>::THREADS, 1)
+router_gemm_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
+                   int N, int D, int E, int kb_per_split,
+                   float* __restrict__ logits, float* __restrict__ partials, int* __restrict__ status) {
+  using C = Cfg<NT>;
+  constexpr uint32_t IDESC_H = idesc_bf16(BM, NT);
+  constexpr uint32_t IDESC_L = idesc_bf16(BM, 2 * NT);
+  constexpr int STAGES = C::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  constexpr int NBUF = C::NBUF;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES);
+  // bars: full[STAGES], empty[STAGES], tfull[NBUF], tempty[NBUF], done, lfull
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 2 * NBUF + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int m0 = blockIdx.x * BM, e0 = blockIdx.y * NT;
+  const int kb0 = blockIdx.z * kb_per_split;
+  const int kb1 = min(D / BK, kb0 + kb_per_split);
+  auto full_bar = [&](int s) { return smem_u32(bars + s); };
+  auto empty_bar = [&](int s) { return smem_u32(bars + STAGES + s); };
+  auto tfull_bar = [&](int a) { return smem_u32(bars + 2 * STAGES + a); };
+  auto tempty_bar = [&](int a) { return smem_u32(bars + 2 * STAGES + NBUF + a); };
+  const uint32_t done_bar = smem_u32(bars + 2 * STAGES + 2 * NBUF);
+  const uint32_t lfull_bar = smem_u32(bars + 2 * STAGES + 2 * NBUF + 1);
+
+  if (t == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < NBUF; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), C::EPI);  // one arrival per epilogue warp
+    }
+    mbar_init(done_bar, 1);
+    mbar_init(lfull_bar, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_holder)),
+                 "r"(C::TMEM_COLS));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, issued = 0, issued_par = 0;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, status, true)) break;
+        const uint32_t a_dst = smem_u32(smem + stage * C::STAGE_BYTES);
+        mbar_expect_tx(full_bar(stage), C::STAGE_BYTES);
+        tma_load_2d(a_dst, &map_x, kb * BK, m0, full_bar(stage));
+#pragma unroll
+        for (int sp = 0; sp < 3; ++sp)
+          tma_load_2d(a_dst + C::A_BYTES + sp * C::B_BYTES, &map_w, kb * BK, sp * E + e0, full_bar(stage));
+        issued |= 1u << stage;
+        issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      }
+      for (int s = 0; s < STAGES; ++s)
+        if ((issued >> s) & 1u) mbar_wait(full_bar(s), (issued_par >> s) & 1u, abort_flag, status, false);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, status, true)) break;
+        if (!mbar_wait(full_bar(stage), phase, abort_flag, status, true)) break;
+        tc_fence_after();
+        const uint32_t a_base = smem_u32(smem + stage * C::STAGE_BYTES);
+        const uint32_t b_base = a_base + C::A_BYTES;  // [hi ; mid ; lo], NT rows each
+#pragma unroll
+        for (int k = 0; k < BK / UK; ++k) {
+          const uint64_t ad = sw128_desc(a_base + k * UK * 2);
+          tc_mma(tmem_base + (uint32_t)(acc * NT), ad, sw128_desc(b_base + k * UK * 2), IDESC_H, k ? 1u : 0u);
+          tc_mma(tmem_base + (uint32_t)C::L_COL, ad, sw128_desc(b_base + C::B_BYTES + k * UK * 2), IDESC_L,
+                 (kb > kb0 || k) ? 1u : 0u);
+        }
+        tc_commit(empty_bar(stage));
+        tc_commit(tfull_bar(acc));
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        if (++acc == NBUF) { acc = 0; acc_phase ^= 1u; }
+      }
+      tc_commit(lfull_bar);
+      tc_commit(done_bar);
+      mbar_wait(done_bar, 0, abort_flag, status, false);
+    }
+  } else {
+    constexpr int W = C::W;
+    const int q = warp & 3;                // TMEM lane quarter
+    const int cb = ((warp - 2) >> 2) * W;  // this warp's first column
+    const int row = m0 + q * 32 + lane;
+    // Slice partials are added plainly into `loc` (8 slices at most), and every 8 slices
+    // `loc` is folded into the running total with a two-sum (s, c).
+    float s[W], c[W], loc[W];
+#pragma unroll
+    for (int j = 0; j < W; ++j) s[j] = c[j] = loc[j] = 0.f;
+    auto fold = [&]() {
+#pragma unroll
+      for (int j = 0; j < W; ++j) {
+        const float a = s[j], b = loc[j];
+        const float tt = a + b;
+        const float bp = tt - a;
+        c[j] += (a - (tt - bp)) + (b - bp);
+        s[j] = tt;
+        loc[j] = 0.f;
+      }
+    };
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int kb = kb0; kb < kb1; ++kb) {
+      // lane 0 watches the barrier; the warp follows through __syncwarp
+      int got = 1;
+      if (lane == 0) got = mbar_wait(tfull_bar(acc), acc_phase, abort_flag, status, true) ? 1 : 0;
+      __syncwarp();
+      ok = __shfl_sync(0xffffffffu, got, 0) != 0;
+      if (!ok) break;
+      tc_fence_after();
+      float p[W];
+      tmem_ld_cols<W>(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * NT + cb), p);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty_bar(acc));
+#pragma unroll
+      for (int j = 0; j < W; ++j) loc[j] += p[j];
+      if (((kb - kb0) & 7) == 7) fold();
+      if (++acc == NBUF) { acc = 0; acc_phase ^= 1u; }
+    }
+    fold();
+    if (ok) {
+      int got = 1;
+      if (lane == 0) got = mbar_wait(lfull_bar, 0, abort_flag, status, true) ? 1 : 0;
+      __syncwarp();
+      ok = __shfl_sync(0xffffffffu, got, 0) != 0;
+    }
+    if (ok) {  // mid and lo plane sums of this thread's columns
+      tc_fence_after();
+      const uint32_t lb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)C::L_COL;
+      float pm[W], pl[W];
+      tmem_ld_cols<W>(lb + (uint32_t)cb, pm);
+      tmem_ld_cols<W>(lb + (uint32_t)(NT + cb), pl);
+#pragma unroll
+      for (int j = 0; j < W; ++j) {
+        const float b = pm[j] + pl[j];
+        const float a = s[j];
+        const float tt = a + b;
+        const float bp = tt - a;
+        c[j] += (a - (tt - bp)) + (b - bp);
+        s[j] = tt;
+      }
+    }
+    if (ok && row < N) {
+      const int e1 = e0 + cb;
+      float* dst = (blockIdx.z == 0 ? logits : partials + (size_t)(blockIdx.z - 1) * N * E) + (size_t)row * E + e1;
+      if (e1 + W <= E && (E & 3) == 0) {
+#pragma unroll
+        for (int j = 0; j < W; j += 4)
+          *reinterpret_cast<float4*>(dst + j) =
+              make_float4(s[j] + c[j], s[j + 1] + c[j + 1], s[j + 2] + c[j + 2], s[j + 3] + c[j + 3]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < W; ++j)
+          if (e1 + j < E) dst[j] = s[j] + c[j];
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(C::TMEM_COLS));
+  }
+}
+
+// warp per token over the logits
+template <int PER>
+__global__ void __launch_bounds__(256) topk_kernel(float* __restrict__ logits, const float* __restrict__ partials,
+                                                   int nsplit, const float* __restrict__ bias, int N, int E, int k,
+                                                   int sigmoid, int32_t* __restrict__ idx, float* __restrict__ gate,
+                                                   uint8_t* __restrict__ tie) {
+  const int lane = threadIdx.x & 31;
+  const int n = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (n >= N) return;
+  float* row = logits + (size_t)n * E;
+  float lg[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int e = lane + 32 * i;
+    lg[i] = e < E ? row[e] : 0.f;
+  }
+  if (nsplit > 1) {  // add the split-K partials in split order (two-sum), write the logits
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int e = lane + 32 * i;
+      if (e >= E) continue;
+      float sum = lg[i], comp = 0.f;
+      for (int z = 1; z < nsplit; ++z) {
+        const float b = partials[((size_t)(z - 1) * N + n) * E + e];
+        const float tt = sum + b;
+        const float bp = tt - sum;
+        comp += (sum - (tt - bp)) + (b - bp);
+        sum = tt;
+      }
+      lg[i] = sum + comp;
+      row[e] = lg[i];
+    }
+  }
+  warp_topk_gates<PER>(lg, lane, E, k, bias, sigmoid, idx + (size_t)n * k, gate + (size_t)n * k,
+                       tie ? tie + n : nullptr);
+}
+
+template <int NT>
+moe_status_t launch_gemm(const CUtensorMap& mx, const CUtensorMap& mw, int N, int D, int E, int nsplit,
+                         float* logits, float* partials, int* status, cudaStream_t s) {
+  auto kern = router_gemm_kernel<NT>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg<NT>::SMEM) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  const int KB = D / BK;
+  const int per = (KB + nsplit - 1) / nsplit;
+  dim3 grid((N + BM - 1) / BM, (E + NT - 1) / NT, nsplit);
+  kern<<<grid, Cfg<NT>::THREADS, Cfg<NT>::SMEM, s>>>(mx, mw, N, D, E, per, logits, partials, status);
+  return launch_status();
+}
+
+// Tile width and split-K count for (N, D, E): about 128 CTAs, at most 4 splits.
+struct Plan {
+  int nt, nsplit;
+};
+
+Plan plan(int N, int D, int E) {
+  Plan p;
+  const int mt = (N + BM - 1) / BM;
+  p.nt = E <= 16 ? 16 : (E <= 32 ? 32 : 64);
+  const int ctas = mt * ((E + p.nt - 1) / p.nt);
+  const int KB = D / BK;
+  p.nsplit = std::max(1, std::min(std::min(4, KB), (128 + ctas - 1) / ctas));
+  // every split must own at least one k-block
+  while (p.nsplit > 1 && (KB + p.nsplit - 1) / p.nsplit * (p.nsplit - 1) >= KB) --p.nsplit;
+  return p;
+}
+
+}  // namespace rtc
+}  // namespace moe
+
+extern "C" size_t moe_router_split_bytes(int E, int D) {
+  if (E <= 0 || D <= 0) return 0;
+  return (size_t)3 * E * D * sizeof(uint16_t);
+}
+
+extern "C" moe_status_t moe_router_split(const float* w_router, int E, int D, void* w_split,
+                                         moe_stream_t stream) {
+  using namespace moe;
+  if (E < 1 || D < 1 || !w_router || !w_split) return MOE_ERR_INVALID_ARG;
+  const long long n = (long long)E * D;
+  const int blocks = (int)std::min<long long>((n + 255) / 256, (long long)sm_count() * 8);
+  rtc::split_kernel<<<blocks, 256, 0, as_cuda(stream)>>>(w_router, n, static_cast<__nv_bfloat16*>(w_split));
+  return launch_status();
+}
+
+extern "C" size_t moe_router_topk_split_workspace_bytes(int N, int D, int E) {
+  if (N <= 0 || D <= 0 || E <= 0 || D % 64 != 0) return 0;
+  const moe::rtc::Plan p = moe::rtc::plan(N, D, E);
+  return (size_t)(p.nsplit - 1) * N * E * sizeof(float);
+}
+
+extern "C" moe_status_t moe_router_topk_split(const void* xn, int N, int D, const void* w_split,
+                                              const float* bias, int E, int k, moe_score_fn_t fn,
+                                              float* logits_out, int32_t* topk_idx, float* topk_gate,
+                                              uint8_t* near_tie, void* workspace, size_t workspace_bytes,
+                                              moe_stream_t stream) {
+  using namespace moe;
+  if (N < 0 || D <= 0 || E < 1 || k < 1 || k > E) return MOE_ERR_INVALID_ARG;
+  if (E > MOE_MAX_EXPERTS || k > MOE_MAX_TOPK || D % 64 != 0) return MOE_ERR_UNSUPPORTED;
+  if (fn != MOE_SCORE_SOFTMAX && fn != MOE_SCORE_SIGMOID) return MOE_ERR_INVALID_ARG;
+  if (N == 0) return MOE_OK;
+  if (!xn || !w_split || !logits_out || !topk_idx || !topk_gate) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(xn) || !aligned16(w_split) || !aligned16(logits_out)) return MOE_ERR_INVALID_ARG;
+  const rtc::Plan p = rtc::plan(N, D, E);
+  if (p.nsplit > 1 && (!workspace || workspace_bytes < moe_router_topk_split_workspace_bytes(N, D, E)))
+    return MOE_ERR_INVALID_ARG;
+  int* status = device_status_word();
+  if (!status) return MOE_ERR_CUDA;
+  cudaStream_t s = as_cuda(stream);
+  CUtensorMap mx, mw;
+  if (!tc::make_map_bf16(&mx, xn, (uint64_t)N, (uint64_t)D, rtc::BM) ||
+      !tc::make_map_bf16(&mw, w_split, (uint64_t)3 * E, (uint64_t)D, (uint32_t)p.nt))
+    return MOE_ERR_CUDA;
+  float* part = static_cast<float*>(workspace);
+  moe_status_t st =
+      p.nt == 16 ? rtc::launch_gemm<16>(mx, mw, N, D, E, p.nsplit, logits_out, part, status, s)
+      : p.nt == 32 ? rtc::launch_gemm<32>(mx, mw, N, D, E, p.nsplit, logits_out, part, status, s)
+                   : rtc::launch_gemm<64>(mx, mw, N, D, E, p.nsplit, logits_out, part, status, s);
+  if (st != MOE_OK) return st;
+  const int sig = fn == MOE_SCORE_SIGMOID;
+  const int grid = (N + 7) / 8;
+#define MOE_TOPK(PER) rtc::topk_kernel<PER><<<grid, 256, 0, s>>>(logits_out, part, p.nsplit, bias, N, E, k, sig, \
+                                                                 topk_idx, topk_gate, near_tie)
+  if (E <= 32) MOE_TOPK(1);
+  else if (E <= 64) MOE_TOPK(2);
+  else if (E <= 128) MOE_TOPK(4);
+  else MOE_TOPK(8);
+#undef MOE_TOPK
+  return launch_status();
+}

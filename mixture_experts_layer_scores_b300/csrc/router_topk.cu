@@ -12,7 +12,7 @@
 // shared memory for a warp-per-token top-k: each lane holds E/32 scores in registers
 // and k+1 rounds of a shuffle arg-max (score desc, id asc) pick the experts and the
 // (k+1)-th score for the near-tie flag.
-#include "moe_internal.cuh"
+#include "topk_common.cuh"
 
 namespace moe {
 namespace {
@@ -90,10 +90,6 @@ struct WLoad {
     }
   }
 };
-
-__device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
-  return va > vb || (va == vb && ia < ib);
-}
 
 template <typename XT, int EP, int TM, int TE>
 __global__ void __launch_bounds__(NT) router_topk_kernel(
@@ -190,70 +186,11 @@ __global__ void __launch_bounds__(NT) router_topk_kernel(
   for (int nl = warp; nl < BT; nl += NT / 32) {
     const int n = n0 + nl;
     if (n >= N) break;
-    float v[PER];
+    float lg[PER];
 #pragma unroll
-    for (int i = 0; i < PER; ++i) {
-      const int e = lane + 32 * i;
-      float key = -INFINITY;
-      if (e < E) {
-        const float lg = lt[nl * (EP + 1) + e];
-        const float sc = sigmoid ? 1.0f / (1.0f + expf(-lg)) : lg;
-        const float sl = sc + (bias ? bias[e] : 0.0f);
-        key = isnan(sl) ? -INFINITY : sl;
-      }
-      v[i] = key;
-    }
-    uint32_t taken = 0;
-    int my_id = 0;
-    float kth = 0.f, next = -INFINITY;
-    const int rounds = k < E ? k + 1 : k;
-    for (int r = 0; r < rounds; ++r) {
-      float bv = -INFINITY;
-      int bi = 0x7fffffff;
-#pragma unroll
-      for (int i = 0; i < PER; ++i) {
-        const int e = lane + 32 * i;
-        if (!((taken >> i) & 1u) && better(v[i], e, bv, bi)) { bv = v[i]; bi = e; }
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-        if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
-      }
-      if (r < k) {
-        if (lane == r) my_id = bi;
-        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-        if (r == k - 1) kth = bv;
-      } else {
-        next = bv;
-      }
-    }
-    // gates over the chosen experts' unbiased scores
-    const bool act = lane < k;
-    const float lg = act ? lt[nl * (EP + 1) + my_id] : 0.f;
-    float g;
-    if (sigmoid) {
-      const float s = act ? 1.0f / (1.0f + expf(-lg)) : 0.f;
-      float sum = s;
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-      g = s / sum;
-    } else {
-      float m = act ? lg : -INFINITY;
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-      const float ex = act ? expf(lg - m) : 0.f;
-      float sum = ex;
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-      g = ex / sum;
-    }
-    if (act) {
-      topk_idx[(size_t)n * k + lane] = my_id;
-      topk_gate[(size_t)n * k + lane] = g;
-    }
-    if (near_tie && lane == 0) near_tie[n] = (k < E && (kth - next) < 1e-6f) ? 1 : 0;
+    for (int i = 0; i < PER; ++i) lg[i] = lt[nl * (EP + 1) + lane + 32 * i];
+    warp_topk_gates<PER>(lg, lane, E, k, bias, sigmoid, topk_idx + (size_t)n * k,
+                         topk_gate + (size_t)n * k, near_tie ? near_tie + n : nullptr);
   }
 }
 

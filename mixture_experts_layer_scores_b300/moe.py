@@ -23,7 +23,8 @@ STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED", -3:
 EXPORTS = ("moe_status_string", "moe_last_device_status", "moe_version", "moe_router_topk",
            "moe_permute_workspace_bytes", "moe_permute", "moe_grouped_swiglu",
            "moe_unpermute_combine", "moe_bias_update", "moe_permute_noalloc",
-           "moe_permute_noalloc_max_scratch_bytes")
+           "moe_permute_noalloc_max_scratch_bytes", "moe_router_split_bytes", "moe_router_split",
+           "moe_router_topk_split", "moe_router_topk_split_workspace_bytes")
 
 
 class MoEError(RuntimeError):
@@ -57,6 +58,10 @@ def load():
         "moe_bias_update": ([vp, i32, i64, f32, vp, vp, vp], i32),
         "moe_permute_noalloc": ([vp, i32, i32, i32, vp, i32, i32, vp, vp, vp, vp, vp, vp], i32),
         "moe_permute_noalloc_max_scratch_bytes": ([], sz),
+        "moe_router_split_bytes": ([i32, i32], sz),
+        "moe_router_split": ([vp, i32, i32, vp, vp], i32),
+        "moe_router_topk_split": ([vp, i32, i32, vp, vp, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp], i32),
+        "moe_router_topk_split_workspace_bytes": ([i32, i32, i32], sz),
     }
     for name, (args, res) in sig.items():
         f = getattr(L, name)
@@ -120,6 +125,47 @@ def moe_router_topk(xn, w_router, bias, k, score_fn="softmax", logits_out=None, 
     _chk("moe_router_topk", L.moe_router_topk(
         _p(xn), _dt(xn), N, D, _p(w_router), _p(bias), E, k, SCORE_FN[score_fn], _p(logits_out),
         _p(topk_idx), _p(topk_gate), _p(near_tie), _stream(stream)))
+    return logits_out, topk_idx, topk_gate, near_tie
+
+
+def moe_router_split(w_router, w_split=None, stream=None):
+    """fp32 [E, D] router weight -> bf16 [3, E, D] planes with hi + mid + lo == w exactly."""
+    L = load()
+    E, D = w_router.shape
+    if w_split is None:
+        w_split = torch.empty(3, E, D, dtype=torch.bfloat16, device=w_router.device)
+    _cuda(w_router, w_split)
+    _chk("moe_router_split", L.moe_router_split(_p(w_router), E, D, _p(w_split), _stream(stream)))
+    return w_split
+
+
+def router_split_workspace_bytes(N, D, E) -> int:
+    return int(load().moe_router_topk_split_workspace_bytes(N, D, E))
+
+
+def moe_router_topk_split(xn, w_split, bias, k, score_fn="softmax", logits_out=None, topk_idx=None,
+                          topk_gate=None, near_tie=None, want_near_tie=True, workspace=None,
+                          stream=None):
+    """The router on tensor cores (bf16 xn, split fp32 weights).  Returns (logits, idx, gate, near_tie)."""
+    L = load()
+    N, D = xn.shape
+    E = w_split.shape[1]
+    dev = xn.device
+    if logits_out is None:
+        logits_out = torch.empty(N, E, dtype=torch.float32, device=dev)
+    if topk_idx is None:
+        topk_idx = torch.empty(N, k, dtype=torch.int32, device=dev)
+    if topk_gate is None:
+        topk_gate = torch.empty(N, k, dtype=torch.float32, device=dev)
+    if near_tie is None and want_near_tie:
+        near_tie = torch.empty(N, dtype=torch.uint8, device=dev)
+    if workspace is None:
+        workspace = torch.empty(max(1, router_split_workspace_bytes(N, D, E)), dtype=torch.uint8,
+                                device=dev)
+    _cuda(xn, w_split, bias, logits_out, topk_idx, topk_gate, near_tie, workspace)
+    _chk("moe_router_topk_split", L.moe_router_topk_split(
+        _p(xn), N, D, _p(w_split), _p(bias), E, k, SCORE_FN[score_fn], _p(logits_out), _p(topk_idx),
+        _p(topk_gate), _p(near_tie), _p(workspace), workspace.numel(), _stream(stream)))
     return logits_out, topk_idx, topk_gate, near_tie
 
 
@@ -257,6 +303,10 @@ class MoELayer:
         self.out = e(N, self.D, dt=dtype)
         self.workspace = e(max(1, permute_workspace_bytes(N, k, self.E)), dt=torch.uint8)
         self.mom = e(1, dt=torch.float32)
+        self.tc_router = dtype == torch.bfloat16
+        self.w_split = e(3, self.E, self.D, dt=torch.bfloat16) if self.tc_router else None
+        self.router_ws = e(max(1, router_split_workspace_bytes(N, self.D, self.E)), dt=torch.uint8) \
+            if self.tc_router else None
         if w.shared is not None:
             Fs = w.shared[0].shape[1]
             self.sh_offsets = torch.tensor([0, N], dtype=torch.int32, device=dev)
@@ -268,8 +318,7 @@ class MoELayer:
     def forward(self, xn, h, update_bias=True, stream=None):
         """out = h + shared(xn) + sum_j gate_j Expert_j(xn); then the +-gamma bias step."""
         w = self.w
-        moe_router_topk(xn, w.w_router, w.bias, self.k, self.score_fn, self.logits, self.idx,
-                        self.gate, self.near_tie, stream=stream)
+        self.route(xn, stream)
         moe_permute(xn, self.idx, self.E, self.counts, self.offsets, self.row_map,
                     self.perm_token, self.x_perm, self.workspace, stream=stream)
         moe_grouped_swiglu(self.x_perm, self.offsets, w.w_gate, w.w_up, w.w_down, self.h_ws,
@@ -284,4 +333,20 @@ class MoELayer:
                             stream=stream)
         return self.out
 
-    kernels_per_forward = property(lambda self: 1 + 4 + 2 + (2 if self.w.shared else 0) + 1 + 1)
+    def route(self, xn, stream=None):
+        """Router + top-k.  bf16 activations: the fp32 router weight is re-split into bf16
+        planes (every call, so weight updates are always seen) and run on tensor cores."""
+        w = self.w
+        if self.tc_router:
+            moe_router_split(w.w_router, self.w_split, stream=stream)
+            moe_router_topk_split(xn, self.w_split, w.bias, self.k, self.score_fn, self.logits,
+                                  self.idx, self.gate, self.near_tie, workspace=self.router_ws,
+                                  stream=stream)
+        else:
+            moe_router_topk(xn, w.w_router, w.bias, self.k, self.score_fn, self.logits, self.idx,
+                            self.gate, self.near_tie, stream=stream)
+
+    @property
+    def kernels_per_forward(self):
+        router = 3 if self.tc_router else 1
+        return router + 4 + 2 + (2 if self.w.shared else 0) + 1 + 1

@@ -66,7 +66,11 @@ def gpu_layer(cfg, inp, k=None, update_bias=True):
     E = cfg.E
     xn = inp["xn"]
     bias = inp["bias"].clone()
-    logits, idx, gate, tie = moe.moe_router_topk(xn, inp["w_router"], bias, k, cfg.score_fn)
+    if xn.dtype == torch.bfloat16:  # the product path: tensor-core router on split weights
+        w_split = moe.moe_router_split(inp["w_router"])
+        logits, idx, gate, tie = moe.moe_router_topk_split(xn, w_split, bias, k, cfg.score_fn)
+    else:
+        logits, idx, gate, tie = moe.moe_router_topk(xn, inp["w_router"], bias, k, cfg.score_fn)
     counts, offsets, row_map, perm, x_perm = moe.moe_permute(xn, idx, E)
     y_perm = moe.moe_grouped_swiglu(x_perm, offsets, inp["w_gate"], inp["w_up"], inp["w_down"])
     sh_y = None
