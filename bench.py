@@ -166,9 +166,8 @@ class Step:
         rec(4)
         moe.moe_unpermute_combine(L.y_perm, L.row_map, L.gate, L.sh_y, h, L.out)
         rec(5)
-        if self.world > 1:
-            torch.distributed.all_reduce(L.counts)  # global load histogram for the bias step
-        moe.moe_bias_update(L.counts, w.bias, L.N * L.k * self.world, L.gamma, L.mom)
+        world = moe.global_counts(L.counts)  # global load histogram for the bias step
+        moe.moe_bias_update(L.counts, w.bias, L.N * L.k * world, L.gamma, L.mom)
         rec(6)
         return L.out
 

@@ -262,6 +262,20 @@ def moe_bias_update(counts, bias, total_assignments, gamma, max_over_mean=None, 
     return max_over_mean
 
 
+def global_counts(counts, group=None):
+    """Data-parallel replicas over tokens: sum the per-expert counts of every replica (one
+    E-element all-reduce, the layer's only cross-replica exchange), so the +-gamma step
+    that follows sees the global load and every replica keeps the same bias.  Returns the
+    number of replicas.  Works on any torch.distributed backend (NCCL on GPUs, gloo on CPU)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return 1
+    world = dist.get_world_size(group)
+    if world > 1:
+        dist.all_reduce(counts, op=dist.ReduceOp.SUM, group=group)
+    return world
+
+
 # ----------------------------------------------------------------------------------------
 # The whole layer: buffers allocated once, then the five calls in order.
 # ----------------------------------------------------------------------------------------

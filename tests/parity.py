@@ -174,22 +174,25 @@ def compare_layer(cfg, g, o, k=None, f32=False):
     return rep
 
 
-def moe_delta_close(cfg, g, o, h, f32=False):
-    """Tolerance on the MoE delta out - h as well (the residual must not hide errors).
+def delta_close(name, out_got, out_want, h, f32=False):
+    """Tolerance on the MoE delta out - h (the residual must not hide expert errors).
 
     The GPU's out is rounded once to the output dtype, so each element of out - h also
     carries up to half an ulp of |out| on top of the expert error; the max-abs bound is
     3e-2 * rms(delta) plus that half ulp (relative Frobenius stays 1e-2)."""
-    got = np64(g["out"]) - h
-    ref = o["out"] - h
+    got = np.asarray(out_got, np.float64) - h
+    ref = np.asarray(out_want, np.float64) - h
     rf, mr = (F32_REL_FRO, F32_MAX_RMS) if f32 else (BF16_REL_FRO, BF16_MAX_RMS)
     a = rel_fro(got, ref)
-    assert a <= rf, f"out - h: rel_fro={a:.3e} (<= {rf})"
+    assert a <= rf, f"{name}: rel_fro={a:.3e} (<= {rf})"
     mant_bits = 24 if f32 else 8
-    _, ex = np.frexp(np.abs(o["out"]))
+    _, ex = np.frexp(np.abs(np.asarray(out_want, np.float64)))
     half_ulp = np.ldexp(1.0, ex - mant_bits - 1)
     rms = float(np.sqrt(np.mean(ref ** 2)))
-    excess = np.abs(got - ref) - half_ulp
-    b = float(np.max(excess) / rms)
-    assert b <= mr, f"out - h: (max abs - half ulp of out)/rms = {b:.3e} (<= {mr})"
+    b = float(np.max(np.abs(got - ref) - half_ulp) / rms)
+    assert b <= mr, f"{name}: (max abs - half ulp of out)/rms = {b:.3e} (<= {mr})"
     return a, b
+
+
+def moe_delta_close(cfg, g, o, h, f32=False):
+    return delta_close("out - h", np64(g["out"]), o["out"], h, f32)

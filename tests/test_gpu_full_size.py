@@ -1,0 +1,122 @@
+"""Full-size layers, in the launch configuration bench.py times (MoELayer, same buffers).
+
+The oracle checks, at each configuration's real size:
+* routing of every token (logits, ids outside the near-tie band, gates);
+* counts, offsets, row map and token permutation, bit for bit;
+* the permuted rows, bit for bit;
+* the expert outputs and the layer output of a seeded sample of tokens, computed one expert
+  at a time on the CPU from regenerated weights (bf16 tolerance of tests/parity.py);
+* the bias step, bit for bit;
+and one property that holds at any size checks the combine over every token:
+out = h + shared + sum_j gate * Y[row_map], evaluated in float64 from the kernel's inputs.
+"""
+import numpy as np
+import pytest
+import torch
+
+from mixture_experts_layer_scores_b300 import moe, synth
+from oracle import moe_oracle
+from tests import parity as P
+
+pytestmark = pytest.mark.gpu
+
+CASES = [("handbook", None), ("mixtral", None), ("deepseek_v3", None), ("skewed", 8), ("skewed", 4)]
+SAMPLE = 6
+
+
+def _layer(cfg, k):
+    dev = "cuda"
+    xn, h = synth.make_tokens(cfg, dev)
+    w_r, b = synth.make_router(cfg, dev)
+    b = synth.gaussian(cfg.seed, "bias", (cfg.E,), 0.02 if cfg.score_fn == "sigmoid" else 0.1, device=dev)
+    wg, wu, wd = synth.make_experts(cfg, dev)
+    sh = synth.make_shared(cfg, dev)
+    b0 = b.clone()
+    layer = moe.MoELayer(moe.LayerWeights(w_r, b, wg, wu, wd, sh), cfg.N, k, cfg.score_fn, cfg.gamma)
+    out = layer.forward(xn, h)
+    torch.cuda.synchronize()
+    assert moe.last_device_status() == 0
+    return layer, xn, h, b0, out
+
+
+@pytest.mark.parametrize("name,k", CASES, ids=[f"{n}-k{k or synth.CONFIGS[n].k}" for n, k in CASES])
+def test_full_size_layer(name, k):
+    cfg = synth.CONFIGS[name]
+    k = cfg.k if k is None else k
+    layer, xn, h, b0, out = _layer(cfg, k)
+
+    # --- routing, every token -------------------------------------------------------
+    xc, hc = synth.make_tokens(cfg, "cpu")
+    wc, _ = synth.make_router(cfg, "cpu")
+    assert torch.equal(xc, xn.cpu()) and torch.equal(hc, h.cpu())   # same generator bits
+    r = moe_oracle.route(P.np64(xc), wc.numpy(), b0.cpu().numpy(), k, cfg.score_fn)
+    g = {"idx": layer.idx.cpu(), "gate": layer.gate.cpu(), "logits": layer.logits.cpu(),
+         "near_tie": layer.near_tie.cpu()}
+    rep = P.compare_routing(g, r, k)
+    print(name, k, rep)
+
+    idx = g["idx"].numpy()
+    same = ~(idx != r["idx"]).any(1)
+    # --- histogram, scan, permutation ------------------------------------------------
+    if rep["identical"]:
+        counts = moe_oracle.expert_counts(r["idx"], cfg.E)
+        offsets = moe_oracle.exclusive_scan(counts)
+        row_map, perm = moe_oracle.stable_permutation(r["idx"], offsets)
+        assert np.array_equal(layer.counts.cpu().numpy(), counts)
+        assert np.array_equal(layer.offsets.cpu().numpy(), offsets)
+        assert np.array_equal(layer.row_map.cpu().numpy(), row_map)
+        assert np.array_equal(layer.perm_token.cpu().numpy(), perm)
+        new_b, mom = moe_oracle.bias_update(b0.cpu().numpy(), counts, cfg.N * k, cfg.gamma)
+        assert np.array_equal(layer.w.bias.cpu().numpy(), new_b)
+        assert abs(layer.mom.item() - mom) <= 1e-6 * mom
+    else:
+        P.check_permutation_properties({"idx": g["idx"], "counts": layer.counts.cpu(),
+                                        "offsets": layer.offsets.cpu(), "row_map": layer.row_map.cpu(),
+                                        "perm_token": layer.perm_token.cpu()}, cfg.E, k)
+    perm_t = layer.perm_token.long()
+    assert torch.equal(layer.x_perm, xn[perm_t])                      # permuted rows exact
+
+    # --- the combine, every token (property) -------------------------------------------
+    rm = layer.row_map.long()
+    ref = h.double() + (layer.sh_y.double() if layer.sh_y is not None else 0.0)
+    ref = ref + (layer.gate.double()[:, :, None] * layer.y_perm.double()[rm]).sum(1)
+    err = (out.double() - ref).abs()
+    half_ulp = torch.ldexp(torch.ones_like(ref), torch.frexp(ref.abs())[1] - 9)
+    assert bool((err <= half_ulp * 1.0001 + 1e-6).all()), float((err - half_ulp).max())
+
+    # --- expert outputs and layer output of sampled tokens ----------------------------
+    rng = np.random.default_rng(cfg.seed)
+    tokens = rng.choice(np.where(same)[0], SAMPLE, replace=False)
+    x_s = P.np64(xc[tokens])
+    want_y = {}                            # (token position, slot) -> oracle expert output
+    for e in sorted({int(v) for v in r["idx"][tokens].ravel()}):
+        wg, wu, wd = (P.np64(t) for t in synth.make_expert(cfg, e, "cpu"))
+        for i, t in enumerate(tokens):
+            for j in np.where(r["idx"][t] == e)[0]:
+                want_y[(i, j)] = moe_oracle.swiglu_expert(x_s[i:i + 1], wg, wu, wd)[0]
+    y_gpu = layer.y_perm.cpu()
+    got_rows, want_rows = [], []
+    for (i, j), y in want_y.items():
+        got_rows.append(P.np64(y_gpu[int(layer.row_map[tokens[i], j])]))
+        want_rows.append(y)
+    P.assert_close("y_perm (sampled rows)", np.stack(got_rows), np.stack(want_rows))
+    want_out = P.np64(hc[tokens]).copy()
+    if cfg.shared:
+        sg, su, sd = synth.make_expert(cfg, 0, "cpu", shared=True)
+        ysh = moe_oracle.swiglu_expert(x_s, P.np64(sg), P.np64(su), P.np64(sd))
+        P.assert_close("shared_y (sampled)", P.np64(layer.sh_y.cpu()[tokens]), ysh)
+        want_out += ysh
+    for (i, j), y in want_y.items():
+        want_out[i] += r["gate"][tokens[i], j] * y
+    P.assert_close("out (sampled)", P.np64(out.cpu()[tokens]), want_out)
+    P.delta_close("out - h (sampled)", P.np64(out.cpu()[tokens]), want_out, P.np64(hc[tokens]))
+
+
+def test_generator_bits_equal_on_gpu_and_cpu():
+    for name in ("handbook", "deepseek_v3"):
+        cfg = synth.CONFIGS[name]
+        idx = torch.arange(0, cfg.E * cfg.F * cfg.D, 9973, dtype=torch.int64)
+        for stream in ("w_gate", "w_down", "xn"):
+            a = synth.gaussian_at(cfg.seed, stream, idx.cuda(), 0.1, torch.bfloat16).cpu()
+            b = synth.gaussian_at(cfg.seed, stream, idx, 0.1, torch.bfloat16)
+            assert torch.equal(a, b)
