@@ -45,6 +45,28 @@ def peaks():
     return FALLBACK_PEAKS, "fallback"
 
 
+def recorded_traffic(cfg):
+    """ncu DRAM bytes of one grouped SwiGLU call, if recorded for this workload and the kernel
+    sources are unchanged since (else None)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", f"grouped_gemm_{cfg.name}_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    kv = {}
+    with open(path) as f:
+        for line in f:
+            if "=" in line and not line.startswith("#"):
+                k, v = line.strip().split("=", 1)
+                kv[k] = v
+    h = hashlib.sha256()
+    for src in kv.get("sources", "").split():
+        with open(os.path.join(ROOT, src), "rb") as f:
+            h.update(f.read())
+    if h.hexdigest() != kv.get("sources_sha256"):
+        return None
+    return int(kv["dram_bytes_per_call"])
+
+
 def workload_name(cfg):
     s = f"{cfg.name}: N={cfg.N} D={cfg.D} E={cfg.E} F={cfg.F} k={cfg.k} {cfg.score_fn}"
     if cfg.shared:
@@ -360,7 +382,11 @@ def main():
     gemm_us = stage_us["grouped_swiglu"]
     gemm_tflops = alg["gemm_flops"] / (gemm_us * 1e-6) / 1e12
     perm_gbs = alg["permute_bytes"] / (stage_us["permute"] * 1e-6) / 1e9
-    peak_t = pk["bf16_tflops"]
+    # a kernel timed inside a loop of a second or more runs under the power cap: compare it
+    # with the sustained bf16 figure; shorter timed regions with the burst figure
+    long_run = total_ms >= 1000.0
+    peak_t = pk["bf16_tflops_sustained"] if long_run else pk["bf16_tflops"]
+    peak_label = f"{pk_kind} bf16 {'sustained' if long_run else 'burst'}"
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -372,8 +398,9 @@ def main():
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": {"kernel": "moe_grouped_swiglu (GEMM1+SwiGLU and GEMM2 launches)", "bound": "tensor",
                      "achieved": gemm_tflops, "peak": peak_t, "unit": "TFLOP/s",
-                     "frac": gemm_tflops / peak_t, "traffic": None,
-                     "peak_kind": f"{pk_kind} bf16 burst"},
+                     "frac": gemm_tflops / peak_t, "traffic": recorded_traffic(cfg),
+                     "traffic_unit": "bytes per call (ncu)", "peak_kind": peak_label,
+                     "frac_of_burst": gemm_tflops / pk["bf16_tflops"]},
         "grouped_gemm_tflops": gemm_tflops,
         "permute_gbs": perm_gbs,
         "permute_frac_hbm": perm_gbs / pk["hbm_gbs"],

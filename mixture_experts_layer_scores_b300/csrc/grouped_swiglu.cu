@@ -50,8 +50,9 @@ struct Tile {
   int g, row0, rows, nb, mb;
 };
 
-__device__ __forceinline__ Tile decode(int tile, const int* tile_start, int G, const int32_t* offsets,
-                                       int M_total, int NB) {
+template <int ROWS>
+__device__ __forceinline__ Tile decode_rows(int tile, const int* tile_start, int G, const int32_t* offsets,
+                                            int M_total, int NB) {
   int lo = 0, hi = G - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -61,14 +62,19 @@ __device__ __forceinline__ Tile decode(int tile, const int* tile_start, int G, c
   t.g = lo;
   const int s = min(max(__ldg(offsets + lo), 0), M_total);
   const int e = min(max(__ldg(offsets + lo + 1), s), M_total);
-  const int mblk = (e - s + BM - 1) / BM;
+  const int mblk = (e - s + ROWS - 1) / ROWS;
   const int local = tile - tile_start[lo];
   t.nb = local / mblk;
   const int mb = local - t.nb * mblk;
   t.mb = mb;
-  t.row0 = s + mb * BM;
-  t.rows = min(BM, e - t.row0);
+  t.row0 = s + mb * ROWS;
+  t.rows = min(ROWS, e - t.row0);
   return t;
+}
+
+__device__ __forceinline__ Tile decode(int tile, const int* tile_start, int G, const int32_t* offsets,
+                                       int M_total, int NB) {
+  return decode_rows<BM>(tile, tile_start, G, offsets, M_total, NB);
 }
 
 // MODE 0: GEMM1 with SwiGLU epilogue (B = gate rows ; up rows, 128 output columns per tile)

@@ -51,10 +51,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // a register read, so polling costs nothing extra.
 static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                               int* status, bool honour_abort) {
-  if (mbar_try_wait(bar, parity)) return true;
+  auto poll = [&]() { return mbar_try_wait(bar, parity); };
+  if (poll()) return true;
   const long long t0 = clock64();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (poll()) return true;
     if ((it & 63u) == 0) {
       if (honour_abort && *abort_flag) return false;
       if (clock64() - t0 > WAIT_LIMIT_CYCLES) {
