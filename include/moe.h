@@ -52,11 +52,19 @@ typedef enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype_t;
  *  MOE_SCORE_SOFTMAX: selection on logit + bias; gates = softmax over the k chosen
  *    raw logits (lesson, "Build it", step 1).
  *  MOE_SCORE_SIGMOID: s = sigmoid(logit); selection on s + bias; gates = s_j / sum of
- *    the chosen s (the sigmoid router the handbook article names, read this way). */
-typedef enum moe_score_fn { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 } moe_score_fn_t;
+ *    the chosen s (the sigmoid router the handbook article names, read this way).
+ *  MOE_SCORE_SQRT_SOFTPLUS: s = sqrt(ln(1 + e^logit)), read like the sigmoid router (the
+ *    third router of the handbook post's question list). */
+typedef enum moe_score_fn {
+  MOE_SCORE_SOFTMAX = 0,
+  MOE_SCORE_SIGMOID = 1,
+  MOE_SCORE_SQRT_SOFTPLUS = 2
+} moe_score_fn_t;
 
-/* Largest E the router/top-k kernel handles, and largest k. */
-#define MOE_MAX_EXPERTS 256
+/* Largest E: 1024 for the tensor-core router, the permute and the grouped GEMM; 256 for
+ * the CUDA-core fp32 router (moe_router_topk).  Largest k: 16. */
+#define MOE_MAX_EXPERTS 1024
+#define MOE_MAX_EXPERTS_CUDA_CORE 256
 #define MOE_MAX_TOPK 16
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -87,7 +95,7 @@ int moe_version(void);
  *                     less than 1e-6 (0 when k == E), or NULL
  * Requires 1 <= k <= min(E, 16), 1 <= E <= 256, D % 64 == 0, N >= 0.
  * Logits are accumulated in fp32 with per-32-element partial sums combined by
- * compensated (two-sum) addition.
+ * compensated (two-sum) addition.  (CUDA cores; see moe_router_topk_split for bf16.)
  */
 moe_status_t moe_router_topk(const void* xn, moe_dtype_t x_dtype, int N, int D,
                              const float* w_router, const float* bias, int E, int k,
@@ -118,7 +126,7 @@ moe_status_t moe_router_split(const float* w_router, int E, int D, void* w_split
  *   logits_out[N, E] fp32 -- REQUIRED here (the top-k reads it back)
  *   workspace moe_router_topk_split_workspace_bytes(N, D, E) bytes (may be 0 / NULL)
  *   bias, topk_idx, topk_gate, near_tie, fn, k: as moe_router_topk.
- * Requires 1 <= k <= min(E, 16), 1 <= E <= 256, D % 64 == 0.
+ * Requires 1 <= k <= min(E, 16), 1 <= E <= 1024, D % 64 == 0.
  */
 size_t moe_router_topk_split_workspace_bytes(int N, int D, int E);
 moe_status_t moe_router_topk_split(const void* xn, int N, int D, const void* w_split,

@@ -285,7 +285,7 @@ router_gemm_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_const
 template <int PER>
 __global__ void __launch_bounds__(256) topk_kernel(float* __restrict__ logits, const float* __restrict__ partials,
                                                    int nsplit, const float* __restrict__ bias, int N, int E, int k,
-                                                   int sigmoid, int32_t* __restrict__ idx, float* __restrict__ gate,
+                                                   int score_fn, int32_t* __restrict__ idx, float* __restrict__ gate,
                                                    uint8_t* __restrict__ tie) {
   const int lane = threadIdx.x & 31;
   const int n = blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -314,7 +314,7 @@ __global__ void __launch_bounds__(256) topk_kernel(float* __restrict__ logits, c
       row[e] = lg[i];
     }
   }
-  warp_topk_gates<PER>(lg, lane, E, k, bias, sigmoid, idx + (size_t)n * k, gate + (size_t)n * k,
+  warp_topk_gates<PER>(lg, lane, E, k, bias, score_fn, idx + (size_t)n * k, gate + (size_t)n * k,
                        tie ? tie + n : nullptr);
 }
 
@@ -380,7 +380,7 @@ extern "C" moe_status_t moe_router_topk_split(const void* xn, int N, int D, cons
   using namespace moe;
   if (N < 0 || D <= 0 || E < 1 || k < 1 || k > E) return MOE_ERR_INVALID_ARG;
   if (E > MOE_MAX_EXPERTS || k > MOE_MAX_TOPK || D % 64 != 0) return MOE_ERR_UNSUPPORTED;
-  if (fn != MOE_SCORE_SOFTMAX && fn != MOE_SCORE_SIGMOID) return MOE_ERR_INVALID_ARG;
+  if (fn != MOE_SCORE_SOFTMAX && fn != MOE_SCORE_SIGMOID && fn != MOE_SCORE_SQRT_SOFTPLUS) return MOE_ERR_INVALID_ARG;
   if (N == 0) return MOE_OK;
   if (!xn || !w_split || !logits_out || !topk_idx || !topk_gate) return MOE_ERR_INVALID_ARG;
   if (!aligned16(xn) || !aligned16(w_split) || !aligned16(logits_out)) return MOE_ERR_INVALID_ARG;
@@ -400,14 +400,16 @@ extern "C" moe_status_t moe_router_topk_split(const void* xn, int N, int D, cons
       : p.nt == 32 ? rtc::launch_gemm<32>(mx, mw, N, D, E, p.nsplit, logits_out, part, status, s)
                    : rtc::launch_gemm<64>(mx, mw, N, D, E, p.nsplit, logits_out, part, status, s);
   if (st != MOE_OK) return st;
-  const int sig = fn == MOE_SCORE_SIGMOID;
+  const int sig = (int)fn;  // score function code
   const int grid = (N + 7) / 8;
 #define MOE_TOPK(PER) rtc::topk_kernel<PER><<<grid, 256, 0, s>>>(logits_out, part, p.nsplit, bias, N, E, k, sig, \
                                                                  topk_idx, topk_gate, near_tie)
   if (E <= 32) MOE_TOPK(1);
   else if (E <= 64) MOE_TOPK(2);
   else if (E <= 128) MOE_TOPK(4);
-  else MOE_TOPK(8);
+  else if (E <= 256) MOE_TOPK(8);
+  else if (E <= 512) MOE_TOPK(16);
+  else MOE_TOPK(32);
 #undef MOE_TOPK
   return launch_status();
 }

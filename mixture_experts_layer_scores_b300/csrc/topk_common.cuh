@@ -2,19 +2,30 @@
 //
 // Lesson "Mixture of Experts", "Build it" step 1: the bias is added to a token's scores
 // only to choose its experts (descending order, ties to the lower id); the gates are a
-// softmax over the chosen experts' original scores.  The sigmoid router reads the same
-// way with s = sigmoid(logit): selection on s + bias, gates s_j / sum of chosen s.
+// softmax over the chosen experts' original scores.  The sigmoid and sqrt(softplus)
+// routers read the same way with s = sigmoid(logit) or s = sqrt(ln(1 + e^logit)):
+// selection on s + bias, gates s_j / sum of the chosen s.
 #pragma once
 
 #include "moe_internal.cuh"
 
 namespace moe {
 
+// score function codes (as moe_score_fn_t)
+enum : int { kScoreSoftmax = 0, kScoreSigmoid = 1, kScoreSqrtSoftplus = 2 };
+
+// Unbiased score s of a logit for the sigmoid / sqrt(softplus) routers.
+__device__ __forceinline__ float router_score(float l, int fn) {
+  if (fn == kScoreSigmoid) return 1.0f / (1.0f + expf(-l));
+  const float sp = fmaxf(l, 0.0f) + log1pf(expf(-fabsf(l)));  // softplus without overflow
+  return sqrtf(sp);
+}
+
 // lg[i] = logit of expert lane + 32 i for this warp's token (entries with id >= E ignored).
 // Lane j < k writes idx_row[j] / gate_row[j]; lane 0 writes *tie_out (if non-null).
 template <int PER>
 __device__ __forceinline__ void warp_topk_gates(const float (&lg)[PER], int lane, int E, int k,
-                                                const float* __restrict__ bias, int sigmoid,
+                                                const float* __restrict__ bias, int score_fn,
                                                 int32_t* __restrict__ idx_row, float* __restrict__ gate_row,
                                                 uint8_t* __restrict__ tie_out) {
   float v[PER];
@@ -23,7 +34,7 @@ __device__ __forceinline__ void warp_topk_gates(const float (&lg)[PER], int lane
     const int e = lane + 32 * i;
     float key = -INFINITY;
     if (e < E) {
-      const float sc = sigmoid ? 1.0f / (1.0f + expf(-lg[i])) : lg[i];
+      const float sc = score_fn == kScoreSoftmax ? lg[i] : router_score(lg[i], score_fn);
       const float sl = sc + (bias ? bias[e] : 0.0f);
       key = isnan(sl) ? -INFINITY : sl;
     }
@@ -71,8 +82,8 @@ __device__ __forceinline__ void warp_topk_gates(const float (&lg)[PER], int lane
   }
   const bool act = lane < k;
   float g;
-  if (sigmoid) {
-    const float s = act ? 1.0f / (1.0f + expf(-my_lg)) : 0.f;
+  if (score_fn != kScoreSoftmax) {
+    const float s = act ? router_score(my_lg, score_fn) : 0.f;
     float sum = s;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);

@@ -17,7 +17,7 @@ _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe.so"
 _lib = None
 
 MOE_F32, MOE_BF16 = 0, 1
-SCORE_FN = {"softmax": 0, "sigmoid": 1}
+SCORE_FN = {"softmax": 0, "sigmoid": 1, "sqrt_softplus": 2}
 STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED", -3: "MOE_ERR_CUDA",
           -4: "MOE_ERR_TIMEOUT", -5: "MOE_ERR_NAN_INPUT"}
 EXPORTS = ("moe_status_string", "moe_last_device_status", "moe_version", "moe_router_topk",

@@ -32,6 +32,8 @@ Readings where the pages leave a step open (each listed again in the design doc):
 
 * Sigmoid router: selection on sigma(logit) + bias, gates sigma_i / sum over the
   chosen sigma_j (unbiased).  No routed scaling factor, no group limit.
+* sqrt(softplus) router (named in the handbook post): read the same way with
+  s = sqrt(ln(1 + e^logit)).
 * Order of the k outputs: descending biased score, ties to the lower expert id
   (a stable sort).  NaN scores rank as -inf.
 * Bias step: b_e <- b_e + gamma * sign(R/E - count_e), sign(0) = 0, in fp32,
@@ -67,7 +69,8 @@ def selection_scores(logits32, bias32, score_fn):
 
     softmax mode: sel = logit + b, gates later from the raw logits.
     sigmoid mode: s = 1 / (1 + exp(-logit)), sel = s + b, gates later from s.
-    Both computed in float64 from the fp32 logit and the fp32 bias.
+    sqrt_softplus mode: s = sqrt(ln(1 + exp(logit))), sel = s + b, gates later from s.
+    All computed in float64 from the fp32 logit and the fp32 bias.
     """
     l64 = np.asarray(logits32, dtype=np.float32).astype(np.float64)
     b64 = np.zeros(l64.shape[-1]) if bias32 is None else \
@@ -76,6 +79,8 @@ def selection_scores(logits32, bias32, score_fn):
         s = l64
     elif score_fn == "sigmoid":
         s = 1.0 / (1.0 + np.exp(-l64))
+    elif score_fn == "sqrt_softplus":
+        s = np.sqrt(np.logaddexp(0.0, l64))
     else:
         raise ValueError(score_fn)
     return s + b64[None, :], s
@@ -102,7 +107,7 @@ def gates(logits32, s_unbiased, idx, score_fn):
     """Gate weights over the chosen experts from their ORIGINAL (unbiased) scores.
 
     softmax mode: g_j = exp(l_j - max) / sum_i exp(l_i - max) over the chosen logits.
-    sigmoid mode: g_j = s_j / sum_i s_i over the chosen sigmoids.
+    sigmoid and sqrt_softplus modes: g_j = s_j / sum_i s_i over the chosen scores.
     """
     rows = np.arange(idx.shape[0])[:, None]
     if score_fn == "softmax":

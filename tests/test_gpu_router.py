@@ -117,3 +117,16 @@ def test_special_scores_order():
     _, idx, _, _ = moe.moe_router_topk_split(x.cuda(), moe.moe_router_split(wf.cuda()), None, 8)
     torch.cuda.synchronize()
     assert idx[0].cpu().tolist() == r["idx"][0].tolist()
+
+
+@pytest.mark.parametrize("N,D,E,k,fn", [(4096, 1024, 896, 16, "sigmoid"), (8192, 2048, 64, 8, "sqrt_softplus"),
+                                        (2048, 512, 1024, 8, "softmax")])
+def test_router_large_E_and_sqrt_softplus(N, D, E, k, fn):
+    """Routers beyond 256 experts (16 of 896, as the handbook article's Kimi example) and the
+    sqrt(softplus) score function, on the tensor-core path."""
+    cfg = synth.scaled(synth.CONFIGS["handbook"], N=N, D=D, E=E, k=k, score_fn=fn)
+    xg, wg, bg, xc, wc, bc = _route_inputs(cfg, 0.02)
+    o = moe_oracle.route(P.np64(xc), wc.numpy(), bc.numpy(), k, fn)
+    tc = moe.moe_router_topk_split(xg, moe.moe_router_split(wg), bg, k, fn)
+    torch.cuda.synchronize()
+    print(N, D, E, k, fn, _check(cfg, tc, o))
