@@ -155,12 +155,32 @@ size_t moe_permute_workspace_bytes(int N, int k, int E);
  * Rows of expert e occupy [offsets[e], offsets[e+1]) in slot order n*k + j (stable).
  * row_map and perm_token must be both given or both NULL; x_perm needs them.
  * An id outside [0, E) sets MOE_ERR_INVALID_ARG in the status word and is skipped.
+ * moe_unpermute_combine skips slots whose row_map is -1.
  */
 moe_status_t moe_permute(const void* xn, moe_dtype_t dtype, int N, int D,
                          const int32_t* topk_idx, int k, int E, int32_t* counts,
                          int32_t* offsets, int32_t* row_map, int32_t* perm_token,
                          void* x_perm, void* workspace, size_t workspace_bytes,
                          moe_stream_t stream);
+
+/*
+ * moe_permute_capacity -- moe_permute with a per-expert capacity (token dropping).
+ * Lesson "Load-balancing problem" item 2: each expert processes at most a fixed number of
+ * tokens and the overflow skips the layer.  Read here per (token, slot) assignment: an
+ * expert keeps the first `capacity` of its slots in slot order n*k + j; every later slot
+ * gets row_map = -1, no row and no copy, so moe_unpermute_combine adds nothing for it (the
+ * remaining gates are not renormalised).  For a capacity factor C use
+ * capacity = ceil(C * N * k / E).
+ *   counts   [E]     the routed demand (before dropping), which drives moe_bias_update
+ *   offsets  [E + 1] exclusive scan of the kept counts min(counts, capacity)
+ * Other arguments as moe_permute; perm_token / x_perm hold offsets[E] <= N*k rows.
+ * capacity >= 0; capacity >= N*k keeps every slot (moe_permute itself).
+ */
+moe_status_t moe_permute_capacity(const void* xn, moe_dtype_t dtype, int N, int D,
+                                  const int32_t* topk_idx, int k, int E, int capacity,
+                                  int32_t* counts, int32_t* offsets, int32_t* row_map,
+                                  int32_t* perm_token, void* x_perm, void* workspace,
+                                  size_t workspace_bytes, moe_stream_t stream);
 
 /*
  * moe_permute_noalloc -- moe_permute without a caller-supplied workspace.

@@ -7,11 +7,13 @@
 //
 // Deterministic, no order-dependent atomics:
 //   1. hist : block b counts the ids of its slot chunk in shared memory -> ws[b][E]
-//   2. scan : one block turns ws into per-block bases (offsets[e] + rows of expert e
-//             in earlier chunks) and writes counts / offsets
+//   2. scan : one block turns ws into per-chunk positions (slots of expert e in earlier
+//             chunks), writes counts (the routed demand) and offsets (exclusive scan of
+//             the kept counts min(count, capacity))
 //   3. rank : block b walks its chunk in slot order; __match_any_sync gives each slot
 //             its rank among same-expert slots of the warp, a per-warp table orders the
-//             warps; row = base + rank.  Writes row_map and perm_token.
+//             warps; position = chunk position + rank, row = offsets[e] + position while
+//             position < capacity, else -1 (dropped).  Writes row_map and perm_token.
 //   4. copy : grid-stride 16-byte row moves xn[n] -> x_perm[row_map[n, j]], each source
 //             vector read once and written k times.
 #include "moe_internal.cuh"
@@ -53,7 +55,7 @@ __global__ void __launch_bounds__(256) hist_kernel(const int32_t* __restrict__ i
 }
 
 // One block of 1024 threads, E <= 1024.  Thread (g, e) owns expert e over chunk range g.
-__global__ void __launch_bounds__(1024) scan_kernel(int32_t* __restrict__ ws, int nb, int E,
+__global__ void __launch_bounds__(1024) scan_kernel(int32_t* __restrict__ ws, int nb, int E, int capacity,
                                                     int32_t* __restrict__ counts,
                                                     int32_t* __restrict__ offsets) {
   extern __shared__ int sh[];  // part[P][E], cnt[E], wsum[32]
@@ -81,8 +83,9 @@ __global__ void __launch_bounds__(1024) scan_kernel(int32_t* __restrict__ ws, in
     cnt[t] = c;
   }
   __syncthreads();
-  // block-wide exclusive scan of cnt[0..E)
-  const int mine = t < E ? cnt[t] : 0;
+  // block-wide exclusive scan of the kept counts min(cnt, capacity)
+  const int demand = t < E ? cnt[t] : 0;
+  const int mine = min(demand, capacity);
   int v = mine;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
@@ -103,15 +106,12 @@ __global__ void __launch_bounds__(1024) scan_kernel(int32_t* __restrict__ ws, in
   __syncthreads();
   const int excl = v - mine + (warp > 0 ? wsum[warp - 1] : 0);
   if (t < E) {
-    counts[t] = mine;
+    counts[t] = demand;
     offsets[t] = excl;
     if (t == E - 1) offsets[E] = excl + mine;
   }
-  __syncthreads();
-  if (t < E) cnt[t] = excl;  // reuse as the expert's first row
-  __syncthreads();
-  if (g < P) {
-    int base = cnt[e] + part[g * E + e];
+  if (g < P) {  // position of chunk b's first slot of expert e within the expert
+    int base = part[g * E + e];
     for (int b = b0; b < b1; ++b) {
       const int x = ws[(size_t)b * E + e];
       ws[(size_t)b * E + e] = base;
@@ -121,7 +121,8 @@ __global__ void __launch_bounds__(1024) scan_kernel(int32_t* __restrict__ ws, in
 }
 
 __global__ void __launch_bounds__(256) rank_kernel(const int32_t* __restrict__ idx, int R, int k,
-                                                   int E, int C, const int32_t* __restrict__ ws,
+                                                   int E, int C, int capacity, const int32_t* __restrict__ ws,
+                                                   const int32_t* __restrict__ offsets,
                                                    int32_t* __restrict__ row_map,
                                                    int32_t* __restrict__ perm_token) {
   extern __shared__ int sh[];
@@ -150,9 +151,14 @@ __global__ void __launch_bounds__(256) rank_kernel(const int32_t* __restrict__ i
     if (e >= 0) {
       int pre = 0;
       for (int w = 0; w < warp; ++w) pre += wcnt[w * E + e];
-      const int row = running[e] + pre + rank;
-      row_map[s] = row;
-      perm_token[row] = s / k;
+      const int pos = running[e] + pre + rank;
+      if (pos < capacity) {
+        const int row = offsets[e] + pos;
+        row_map[s] = row;
+        perm_token[row] = s / k;
+      } else {
+        row_map[s] = -1;  // over capacity: this slot skips the expert
+      }
     } else if (s < s1) {
       row_map[s] = -1;
     }
@@ -206,13 +212,13 @@ extern "C" size_t moe_permute_workspace_bytes(int N, int k, int E) {
   return (size_t)p.nb * (size_t)E * sizeof(int32_t);
 }
 
-extern "C" moe_status_t moe_permute(const void* xn, moe_dtype_t dtype, int N, int D,
-                                    const int32_t* topk_idx, int k, int E, int32_t* counts,
-                                    int32_t* offsets, int32_t* row_map, int32_t* perm_token,
-                                    void* x_perm, void* workspace, size_t workspace_bytes,
-                                    moe_stream_t stream) {
+extern "C" moe_status_t moe_permute_capacity(const void* xn, moe_dtype_t dtype, int N, int D,
+                                             const int32_t* topk_idx, int k, int E, int capacity,
+                                             int32_t* counts, int32_t* offsets, int32_t* row_map,
+                                             int32_t* perm_token, void* x_perm, void* workspace,
+                                             size_t workspace_bytes, moe_stream_t stream) {
   using namespace moe;
-  if (N < 0 || k < 1 || E < 1 || k > E || D <= 0) return MOE_ERR_INVALID_ARG;
+  if (N < 0 || k < 1 || E < 1 || k > E || D <= 0 || capacity < 0) return MOE_ERR_INVALID_ARG;
   if (E > 1024 || (long long)N * k >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
   if (dtype != MOE_BF16 && dtype != MOE_F32) return MOE_ERR_UNSUPPORTED;
   if (!counts || !offsets) return MOE_ERR_INVALID_ARG;
@@ -237,10 +243,11 @@ extern "C" moe_status_t moe_permute(const void* xn, moe_dtype_t dtype, int N, in
   int32_t* ws = static_cast<int32_t*>(workspace);
   hist_kernel<<<p.nb, 256, E * sizeof(int), s>>>(topk_idx, R, E, C, ws, status);
   const int P = 1024 / E;
-  scan_kernel<<<1, 1024, (size_t)(P * E + E + 32) * sizeof(int), s>>>(ws, p.nb, E, counts, offsets);
+  scan_kernel<<<1, 1024, (size_t)(P * E + E + 32) * sizeof(int), s>>>(ws, p.nb, E, capacity, counts,
+                                                                        offsets);
   if (row_map) {
-    rank_kernel<<<p.nb, 256, (size_t)9 * E * sizeof(int), s>>>(topk_idx, R, k, E, C, ws, row_map,
-                                                                perm_token);
+    rank_kernel<<<p.nb, 256, (size_t)9 * E * sizeof(int), s>>>(topk_idx, R, k, E, C, capacity, ws, offsets,
+                                                                row_map, perm_token);
   }
   if (x_perm) {
     const int V = (int)(D * esize / 16);
@@ -252,6 +259,15 @@ extern "C" moe_status_t moe_permute(const void* xn, moe_dtype_t dtype, int N, in
                                             static_cast<uint4*>(x_perm));
   }
   return launch_status();
+}
+
+extern "C" moe_status_t moe_permute(const void* xn, moe_dtype_t dtype, int N, int D,
+                                    const int32_t* topk_idx, int k, int E, int32_t* counts,
+                                    int32_t* offsets, int32_t* row_map, int32_t* perm_token,
+                                    void* x_perm, void* workspace, size_t workspace_bytes,
+                                    moe_stream_t stream) {
+  return moe_permute_capacity(xn, dtype, N, D, topk_idx, k, E, 0x7fffffff, counts, offsets, row_map,
+                              perm_token, x_perm, workspace, workspace_bytes, stream);
 }
 
 // ---- moe_permute_noalloc ---------------------------------------------------------------

@@ -24,7 +24,7 @@ EXPORTS = ("moe_status_string", "moe_last_device_status", "moe_version", "moe_ro
            "moe_permute_workspace_bytes", "moe_permute", "moe_grouped_swiglu",
            "moe_unpermute_combine", "moe_bias_update", "moe_permute_noalloc",
            "moe_permute_noalloc_max_scratch_bytes", "moe_router_split_bytes", "moe_router_split",
-           "moe_router_topk_split", "moe_router_topk_split_workspace_bytes")
+           "moe_router_topk_split", "moe_router_topk_split_workspace_bytes", "moe_permute_capacity")
 
 
 class MoEError(RuntimeError):
@@ -56,6 +56,7 @@ def load():
         "moe_grouped_swiglu": ([vp, i32, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp], i32),
         "moe_unpermute_combine": ([vp, vp, vp, i32, i32, i32, vp, vp, vp, i32, vp], i32),
         "moe_bias_update": ([vp, i32, i64, f32, vp, vp, vp], i32),
+        "moe_permute_capacity": ([vp, i32, i32, i32, vp, i32, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp], i32),
         "moe_permute_noalloc": ([vp, i32, i32, i32, vp, i32, i32, vp, vp, vp, vp, vp, vp], i32),
         "moe_permute_noalloc_max_scratch_bytes": ([], sz),
         "moe_router_split_bytes": ([i32, i32], sz),
@@ -173,9 +174,16 @@ def permute_workspace_bytes(N, k, E) -> int:
     return int(load().moe_permute_workspace_bytes(N, k, E))
 
 
+def expert_capacity(capacity_factor, N, k, E) -> int:
+    """Slots per expert for a capacity factor C: ceil(C * N * k / E)."""
+    import math
+    return int(math.ceil(capacity_factor * N * k / E))
+
+
 def moe_permute(xn, topk_idx, E, counts=None, offsets=None, row_map=None, perm_token=None,
-                x_perm=None, workspace=None, rows=True, copy=True, stream=None):
-    """Histogram + scan + stable permutation.  Returns (counts, offsets, row_map, perm_token, x_perm)."""
+                x_perm=None, workspace=None, rows=True, copy=True, capacity=None, stream=None):
+    """Histogram + scan + stable permutation (with an optional per-expert capacity).
+    Returns (counts, offsets, row_map, perm_token, x_perm)."""
     L = load()
     N, k = topk_idx.shape
     dev = topk_idx.device
@@ -194,10 +202,16 @@ def moe_permute(xn, topk_idx, E, counts=None, offsets=None, row_map=None, perm_t
         workspace = torch.empty(max(1, permute_workspace_bytes(N, k, E)), dtype=torch.uint8, device=dev)
     dt = _dt(xn) if xn is not None else MOE_BF16
     _cuda(xn, topk_idx, counts, offsets, row_map, perm_token, x_perm, workspace)
-    _chk("moe_permute", L.moe_permute(
-        _p(xn) if copy else None, dt, N, D, _p(topk_idx), k, E, _p(counts), _p(offsets),
-        _p(row_map), _p(perm_token), _p(x_perm) if copy else None, _p(workspace),
-        workspace.numel() * workspace.element_size(), _stream(stream)))
+    if capacity is None:
+        _chk("moe_permute", L.moe_permute(
+            _p(xn) if copy else None, dt, N, D, _p(topk_idx), k, E, _p(counts), _p(offsets),
+            _p(row_map), _p(perm_token), _p(x_perm) if copy else None, _p(workspace),
+            workspace.numel() * workspace.element_size(), _stream(stream)))
+    else:
+        _chk("moe_permute_capacity", L.moe_permute_capacity(
+            _p(xn) if copy else None, dt, N, D, _p(topk_idx), k, E, int(capacity), _p(counts),
+            _p(offsets), _p(row_map), _p(perm_token), _p(x_perm) if copy else None, _p(workspace),
+            workspace.numel() * workspace.element_size(), _stream(stream)))
     return counts, offsets, row_map, perm_token, x_perm
 
 
@@ -294,9 +308,11 @@ class MoELayer:
     """Top-k MoE FFN layer forward on one GPU, with reusable device buffers."""
 
     def __init__(self, weights: LayerWeights, N: int, k: int, score_fn="softmax", gamma=1e-3,
-                 dtype=torch.bfloat16):
+                 dtype=torch.bfloat16, capacity_factor=None):
         w = weights
         self.w, self.k, self.score_fn, self.gamma = w, k, score_fn, gamma
+        E = w.w_router.shape[0]
+        self.capacity = None if capacity_factor is None else expert_capacity(capacity_factor, N, k, E)
         self.N = N
         self.E, self.D = w.w_router.shape
         self.F = w.w_gate.shape[1]
@@ -334,7 +350,8 @@ class MoELayer:
         w = self.w
         self.route(xn, stream)
         moe_permute(xn, self.idx, self.E, self.counts, self.offsets, self.row_map,
-                    self.perm_token, self.x_perm, self.workspace, stream=stream)
+                    self.perm_token, self.x_perm, self.workspace, capacity=self.capacity,
+                    stream=stream)
         moe_grouped_swiglu(self.x_perm, self.offsets, w.w_gate, w.w_up, w.w_down, self.h_ws,
                            self.y_perm, stream=stream)
         if w.shared is not None:

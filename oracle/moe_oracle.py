@@ -146,24 +146,39 @@ def exclusive_scan(counts):
     return off
 
 
-def stable_permutation(idx, offsets):
+def stable_permutation(idx, offsets, capacity=None):
     """Counting sort of slots by expert, stable in slot order.
 
     Slot s = n*k + j goes to row offsets[e] + (#earlier slots with the same e).
-    Returns row_map[N, k] (slot -> row) and perm_token[R] (row -> token).
+    Returns row_map[N, k] (slot -> row) and perm_token (row -> token).
+
+    With a per-expert capacity [Lesson, "Load-balancing problem" item 2: each expert takes at
+    most so many tokens, the overflow skips the layer], only the first `capacity` slots of an
+    expert (in slot order) get a row; the others get row -1.  `offsets` must then be the
+    exclusive scan of the kept counts min(count, capacity).
     """
     idx = np.asarray(idx)
     N, k = idx.shape
     nxt = np.array(offsets[:-1], dtype=np.int64).copy()
+    seen = np.zeros(len(offsets) - 1, dtype=np.int64)
     row_map = np.empty((N, k), dtype=np.int64)
-    perm_token = np.empty(N * k, dtype=np.int64)
+    perm_token = np.empty(int(offsets[-1]), dtype=np.int64)
     for n in range(N):
         for j in range(k):
             e = idx[n, j]
-            row_map[n, j] = nxt[e]
-            perm_token[nxt[e]] = n
-            nxt[e] += 1
+            if capacity is not None and seen[e] >= capacity:
+                row_map[n, j] = -1
+            else:
+                row_map[n, j] = nxt[e]
+                perm_token[nxt[e]] = n
+                nxt[e] += 1
+            seen[e] += 1
     return row_map, perm_token
+
+
+def expert_capacity(capacity_factor, N, k, E):
+    """Slots per expert for a capacity factor C: ceil(C * N * k / E)."""
+    return int(np.ceil(capacity_factor * N * k / E))
 
 
 # --------------------------------------------------------------------------------------
@@ -202,8 +217,10 @@ def combine(y_perm, row_map, gate, residual=None, shared_y=None):
         out += np.asarray(residual, dtype=np.float64)
     if shared_y is not None:
         out += np.asarray(shared_y, dtype=np.float64)
+    g = np.asarray(gate, dtype=np.float64)
     for j in range(k):
-        out += np.asarray(gate, dtype=np.float64)[:, j:j + 1] * y_perm[row_map[:, j]]
+        kept = np.where(row_map[:, j] >= 0)[0]        # a dropped slot (row -1) adds nothing
+        out[kept] += g[kept, j:j + 1] * y_perm[row_map[kept, j]]
     return out
 
 
@@ -230,11 +247,13 @@ def bias_update(bias32, counts, total_assignments, gamma):
 # --------------------------------------------------------------------------------------
 
 def moe_layer(xn, h, w_router, bias, w_gate, w_up, w_down, k, score_fn="softmax",
-              shared=None, gamma=None, idx_override=None, gate_override=None):
+              shared=None, gamma=None, idx_override=None, gate_override=None, capacity=None):
     """The whole forward on CPU.  Returns every intermediate the CUDA path exposes.
 
     ``shared`` = (w_gate[1,Fs,D], w_up[1,Fs,D], w_down[1,D,Fs]) or None.
     ``idx_override`` / ``gate_override`` replace the router's choice (routing replay).
+    ``capacity`` = slots kept per expert (None: no limit); ``counts`` stays the routed
+    demand, which drives the bias step.
     """
     xn = np.asarray(xn, dtype=np.float64)
     E = np.asarray(w_router).shape[0]
@@ -242,8 +261,9 @@ def moe_layer(xn, h, w_router, bias, w_gate, w_up, w_down, k, score_fn="softmax"
     idx = r["idx"] if idx_override is None else np.asarray(idx_override, dtype=np.int32)
     g = r["gate"] if gate_override is None else np.asarray(gate_override, dtype=np.float64)
     counts = expert_counts(idx, E)
-    offsets = exclusive_scan(counts)
-    row_map, perm_token = stable_permutation(idx, offsets)
+    kept = counts if capacity is None else np.minimum(counts, capacity)
+    offsets = exclusive_scan(kept)
+    row_map, perm_token = stable_permutation(idx, offsets, capacity)
     x_perm = xn[perm_token]
     y_perm = grouped_swiglu(x_perm, offsets, w_gate, w_up, w_down)
     y_sh = None

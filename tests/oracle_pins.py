@@ -249,6 +249,44 @@ def check_bias_dynamics(o):
     assert b[0] == b.min()
 
 
+def check_capacity(o):
+    """Expert capacity (lesson, load-balancing item 2): hand example, the no-op and the
+    drop-everything limits, and the kept set = first `capacity` slots per expert."""
+    # five tokens, k = 1, all to expert 0; capacity 2 keeps tokens 0 and 1
+    idx = np.zeros((5, 1), np.int32)
+    counts = o.expert_counts(idx, 2)
+    off = o.exclusive_scan(np.minimum(counts, 2))
+    rm, pt = o.stable_permutation(idx, off, 2)
+    assert rm.ravel().tolist() == [0, 1, -1, -1, -1] and pt.tolist() == [0, 1]
+    assert o.expert_capacity(1.0, 8, 2, 4) == 4 and o.expert_capacity(1.25, 10, 2, 4) == 7
+    rng = np.random.default_rng(81)
+    N, D, E, k, F = 40, 16, 6, 2, 8
+    x, h = _rand(82, N, D), _rand(83, N, D)
+    w = _rand(84, E, D)
+    wg, wu, wd = _rand(85, E, F, D, scale=.3), _rand(86, E, F, D, scale=.3), _rand(87, E, D, F, scale=.3)
+    full = o.moe_layer(x, h, w, None, wg, wu, wd, k)
+    big = o.moe_layer(x, h, w, None, wg, wu, wd, k, capacity=N * k)
+    assert np.array_equal(big["row_map"], full["row_map"]) and np.allclose(big["out"], full["out"], atol=0)
+    none = o.moe_layer(x, h, w, None, wg, wu, wd, k, capacity=0)
+    assert np.all(none["row_map"] == -1) and np.allclose(none["out"], h, atol=0)
+    cap = 9
+    r = o.moe_layer(x, h, w, None, wg, wu, wd, k, capacity=cap)
+    assert np.array_equal(r["counts"], full["counts"])          # demand, before dropping
+    flat_e, flat_r = r["idx"].ravel(), r["row_map"].ravel()
+    for e in range(E):
+        slots = np.where(flat_e == e)[0]
+        assert np.all(flat_r[slots[:cap]] >= 0) and np.all(flat_r[slots[cap:]] == -1)
+    # a dropped slot contributes nothing; kept slots contribute gate * expert output
+    want = h.astype(np.float64).copy()
+    for n in range(N):
+        for j in range(k):
+            if r["row_map"][n, j] >= 0:
+                e = r["idx"][n, j]
+                want[n] += r["gate"][n, j] * o.swiglu_expert(x[n:n + 1], wg[e], wu[e], wd[e])[0]
+    assert np.allclose(r["out"], want, rtol=1e-12, atol=1e-12)
+
+
 ALL_CHECKS = [check_route_golden, check_layer_golden, check_dense_reduction, check_split_dense,
               check_all_chosen, check_logits_exact, check_library_equivalents,
-              check_bruteforce_topk, check_invariants, check_bias_update_rule, check_bias_dynamics]
+              check_bruteforce_topk, check_invariants, check_bias_update_rule, check_bias_dynamics,
+              check_capacity]

@@ -157,3 +157,45 @@ def test_bias_loop_50_steps():
     assert len(mm_g) >= 10
     assert np.allclose(mm_g, mm_o[:len(mm_g)], rtol=1e-6)
     assert mm_g[-1] < mm_g[0]
+
+
+@pytest.mark.parametrize("factor", [1.0, 1.25, 0.5])
+def test_capacity_dropping(factor):
+    """Expert capacity (lesson, load-balancing item 2) on the skewed router, where popular
+    experts overflow: kept rows, dropped slots, offsets, counts and the layer output match the
+    oracle; the grouped GEMM and the combine run over the kept rows only."""
+    cfg = synth.scaled(C["skewed"], N=1024, D=256, E=32, F=128, k=4)
+    cap = moe.expert_capacity(factor, cfg.N, cfg.k, cfg.E)
+    gi = P.make_inputs(cfg, "cuda")
+    L = moe.MoELayer(moe.LayerWeights(gi["w_router"], gi["bias"].clone(), gi["w_gate"], gi["w_up"],
+                                      gi["w_down"], None), cfg.N, cfg.k, cfg.score_fn, cfg.gamma,
+                     capacity_factor=factor)
+    out = L.forward(gi["xn"], gi["h"])
+    torch.cuda.synchronize()
+    assert moe.last_device_status() == 0
+    ci = P.make_inputs(cfg, "cpu")
+    o = moe_oracle.moe_layer(P.np64(ci["xn"]), P.np64(ci["h"]), ci["w_router"].numpy(), ci["bias"].numpy(),
+                             P.np64(ci["w_gate"]), P.np64(ci["w_up"]), P.np64(ci["w_down"]), cfg.k,
+                             cfg.score_fn, gamma=cfg.gamma, capacity=cap)
+    assert np.array_equal(L.idx.cpu().numpy(), o["idx"])
+    dropped = int((o["row_map"] < 0).sum())
+    if factor <= 1.0:
+        assert dropped > 0  # the skewed router overflows its popular experts
+    assert np.array_equal(L.counts.cpu().numpy(), o["counts"])
+    assert np.array_equal(L.offsets.cpu().numpy(), o["offsets"])
+    assert np.array_equal(L.row_map.cpu().numpy(), o["row_map"])
+    kept = int(o["offsets"][-1])
+    assert np.array_equal(L.perm_token[:kept].cpu().numpy(), o["perm_token"])
+    assert np.array_equal(L.w.bias.cpu().numpy(), o["bias_new"])       # demand drives the bias
+    P.assert_close("y_perm (kept rows)", P.np64(L.y_perm[:kept].cpu()), o["y_perm"])
+    P.assert_close("out", P.np64(out.cpu()), o["out"])
+    # a token that lost every slot gets exactly its residual back; tokens that kept every
+    # slot get the usual bound on the MoE delta (dropping makes the delta's rms over all
+    # tokens meaningless as a scale)
+    none_kept = (o["row_map"] < 0).all(1)
+    all_kept = (o["row_map"] >= 0).all(1)
+    assert torch.equal(out.cpu()[torch.from_numpy(none_kept)], ci["h"][torch.from_numpy(none_kept)])
+    P.delta_close("out - h (tokens with every slot kept)", P.np64(out.cpu())[all_kept], o["out"][all_kept],
+                  P.np64(ci["h"])[all_kept])
+    print("capacity factor", factor, "capacity", cap, "dropped slots", dropped, "of", cfg.N * cfg.k,
+          "tokens with no slot kept", int(none_kept.sum()))
