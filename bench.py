@@ -74,8 +74,9 @@ def workload_name(cfg):
     return s
 
 
-def algorithmic(cfg, k=None):
-    """Algorithmic flops and bytes of each step (only what the method must move)."""
+def algorithmic(cfg, k=None, copy_rows=False):
+    """Algorithmic flops and bytes of each step (only what the method must move).  The
+    permute moves token rows only when the first GEMM does not gather them itself."""
     k = cfg.k if k is None else k
     N, D, E, F, S = cfg.N, cfg.D, cfg.E, cfg.F, cfg.shared
     R = N * k
@@ -84,7 +85,7 @@ def algorithmic(cfg, k=None):
     return dict(
         router_flops=2.0 * N * D * E,
         router_bytes=N * D * b + E * D * 4 + N * E * 4 + N * k * 8 + N,
-        permute_bytes=N * D * b + R * D * b + 12.0 * R,
+        permute_bytes=(N * D * b + R * D * b if copy_rows else 0) + 12.0 * R,
         gemm_flops=6.0 * R * D * F,
         gemm_bytes=3.0 * E * D * F * b + R * D * b + 2.0 * R * F * b + R * D * b,
         shared_flops=6.0 * N * D * Fs * S,
@@ -157,7 +158,7 @@ class Step:
 
     STAGES = ("router", "permute", "grouped_swiglu", "shared", "combine", "bias")
 
-    def __init__(self, cfg, dev, rank, world):
+    def __init__(self, cfg, dev, rank, world, gather=False):
         self.cfg, self.dev, self.world = cfg, dev, world
         seed_tok = cfg.seed + 1000 * rank
         xn, h = synth.make_tokens(cfg, dev, seed=seed_tok)
@@ -166,30 +167,27 @@ class Step:
         wg, wu, wd = synth.make_experts(cfg, dev)
         sh = synth.make_shared(cfg, dev)
         self.layer = moe.MoELayer(moe.LayerWeights(w_r, b, wg, wu, wd, sh), cfg.N, cfg.k,
-                                  cfg.score_fn, cfg.gamma)
+                                  cfg.score_fn, cfg.gamma, gather=gather)
         self.ev = None
 
     def run(self, xn=None, h=None, events=None):
-        L, w = self.layer, self.layer.w
+        L = self.layer
         xn = self.xn if xn is None else xn
         h = self.h if h is None else h
         rec = (lambda i: events[i].record()) if events is not None else (lambda i: None)
         rec(0)
         L.route(xn)
         rec(1)
-        moe.moe_permute(xn, L.idx, L.E, L.counts, L.offsets, L.row_map, L.perm_token, L.x_perm,
-                        L.workspace)
+        L.permute(xn)
         rec(2)
-        moe.moe_grouped_swiglu(L.x_perm, L.offsets, w.w_gate, w.w_up, w.w_down, L.h_ws, L.y_perm)
+        L.experts(xn)
         rec(3)
-        if w.shared is not None:
-            moe.moe_grouped_swiglu(xn, L.sh_offsets, w.shared[0], w.shared[1], w.shared[2], L.sh_h,
-                                   L.sh_y)
+        L.shared_expert(xn)
         rec(4)
-        moe.moe_unpermute_combine(L.y_perm, L.row_map, L.gate, L.sh_y, h, L.out)
+        L.combine(h)
         rec(5)
         world = moe.global_counts(L.counts)  # global load histogram for the bias step
-        moe.moe_bias_update(L.counts, w.bias, L.N * L.k * world, L.gamma, L.mom)
+        L.bias_step(world)
         rec(6)
         return L.out
 
@@ -347,6 +345,9 @@ def main():
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--gather", action="store_true",
+                    help="GEMM1 gathers its rows from xn through perm_token (no x_perm); "
+                         "default: the permute writes x_perm and GEMM1 loads it by TMA")
     args = ap.parse_args()
     cfg = synth.CONFIGS[args.config]
     if args.impl == "reference":
@@ -363,7 +364,7 @@ def main():
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
     dev = torch.device("cuda", local)
 
-    step = Step(cfg, dev, rank, world)
+    step = Step(cfg, dev, rank, world, gather=args.gather)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         total_ms, stage_us = time_device(step, args.steps, args.warmup, world)
@@ -377,7 +378,7 @@ def main():
     ms_step = total_ms / args.steps
     tokens = cfg.N * world
     value = tokens / (ms_step * 1e-3)
-    alg = algorithmic(cfg)
+    alg = algorithmic(cfg, copy_rows=not step.layer.gather)
     pk, pk_kind = peaks()
     gemm_us = stage_us["grouped_swiglu"]
     gemm_tflops = alg["gemm_flops"] / (gemm_us * 1e-6) / 1e12
@@ -395,6 +396,7 @@ def main():
         "config": {"workload": workload_name(cfg), "tokens_per_gpu": cfg.N,
                    "l2": "inputs larger than L2: every step streams %.0f MB of expert weights"
                          % (3 * cfg.E * cfg.D * cfg.F * 2 / 1e6),
+                   "gemm1_rows": "gathered from xn" if step.layer.gather else "permuted copy x_perm",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": {"kernel": "moe_grouped_swiglu (GEMM1+SwiGLU and GEMM2 launches)", "bound": "tensor",
                      "achieved": gemm_tflops, "peak": peak_t, "unit": "TFLOP/s",

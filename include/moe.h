@@ -72,7 +72,8 @@ const char* moe_status_string(moe_status_t status);
 
 /* Waits for `stream`, then returns and clears the status word of the current device:
  * MOE_OK, MOE_ERR_TIMEOUT (a pipeline wait gave up) or MOE_ERR_INVALID_ARG (an
- * expert id outside [0, E) reached moe_permute). */
+ * expert id outside [0, E) reached moe_permute, or a token index outside [0, N)
+ * reached moe_grouped_swiglu_gather). */
 moe_status_t moe_last_device_status(moe_stream_t stream);
 
 /* Library version, major*10000 + minor*100 + patch. */
@@ -228,6 +229,28 @@ moe_status_t moe_grouped_swiglu(const void* x_perm, moe_dtype_t dtype, const int
                                 int G, int M_total, int D, int F, const void* w_gate,
                                 const void* w_up, const void* w_down, void* h_workspace,
                                 void* y_perm, moe_stream_t stream);
+
+/*
+ * moe_grouped_swiglu_gather -- moe_grouped_swiglu with the permutation folded into
+ * the first GEMM: row i of expert input is read straight from xn[perm_token[i]], so
+ * the permuted copy x_perm is never written.  Same arithmetic as moe_grouped_swiglu
+ * on x_perm = xn[perm_token] (bit-identical H and Y).  Lesson "Concept" (experts
+ * see their tokens only); the handbook news article's measurement of permute cost
+ * against the expert GEMMs is why the copy is worth removing.
+ *
+ *   xn          [N, D]        bf16 activations (row stride D)
+ *   perm_token  [M_total]     DEVICE int32 token of each permuted row, in [0, N)
+ *                             for rows [0, offsets[G]) (from moe_permute)
+ *   offsets, w_gate, w_up, w_down, h_workspace, y_perm: as for moe_grouped_swiglu
+ * bf16 only (tcgen05 path).  Requires D % 64 == 0, F % 64 == 0, 1 <= G, N >= 1 when
+ * M_total > 0; xn and every matrix 16-byte aligned.  A perm_token value outside
+ * [0, N) is used as a zero row and sets MOE_ERR_INVALID_ARG in the status word
+ * (moe_permute writes only valid ones).
+ */
+moe_status_t moe_grouped_swiglu_gather(const void* xn, int N, const int32_t* perm_token,
+                                       const int32_t* offsets, int G, int M_total, int D, int F,
+                                       const void* w_gate, const void* w_up, const void* w_down,
+                                       void* h_workspace, void* y_perm, moe_stream_t stream);
 
 /*
  * moe_unpermute_combine -- gather each token's k expert outputs and mix them.

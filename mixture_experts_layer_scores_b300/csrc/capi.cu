@@ -46,7 +46,7 @@ extern "C" moe_status_t moe_last_device_status(moe_stream_t stream) {
   if (cudaMemsetAsync(w, 0, sizeof(int), s) != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
   if (host & moe::kStatusTimeout) return MOE_ERR_TIMEOUT;
-  if (host & moe::kStatusBadExpertId) return MOE_ERR_INVALID_ARG;
+  if (host & (moe::kStatusBadExpertId | moe::kStatusBadToken)) return MOE_ERR_INVALID_ARG;
   return MOE_OK;
 }
 

@@ -79,21 +79,39 @@ __device__ __forceinline__ Tile decode(int tile, const int* tile_start, int G, c
 
 // MODE 0: GEMM1 with SwiGLU epilogue (B = gate rows ; up rows, 128 output columns per tile)
 // MODE 1: GEMM2 (B = 256 rows of W_down, 256 output columns per tile)
+// MODE 2: MODE 0 with the A rows gathered from xn through perm_token (no permuted copy).
+//         Warps 6..9 copy 32 tile rows each with 16-byte cp.async into the 128-byte-swizzled
+//         K-major layout the MMA descriptors expect; each thread keeps LAG k-blocks of copies
+//         in flight, then waits for the oldest, fences the async proxy and arrives on that
+//         stage's full barrier (initialised for 1 + 128 arrivals).  Warp 0 loads only B.
+//         LAG <= STAGES - 2 keeps one k-block queued on the tensor pipe while a stage fills:
+//         the arrival for stage s needs the MMA of stage s + LAG - STAGES to have completed.
 template <int MODE>
-__global__ void __launch_bounds__(THREADS, 1)
+constexpr int kThreads = MODE == 2 ? THREADS + 128 : THREADS;
+#ifndef MOE_GATHER_LAG
+#define MOE_GATHER_LAG (STAGES - 2)
+#endif
+constexpr int GATHER_LAG = MOE_GATHER_LAG;
+static_assert(GATHER_LAG >= 0 && GATHER_LAG < STAGES, "gather lag must leave a stage to wait on");
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads<MODE>, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b0,
                     const __grid_constant__ CUtensorMap map_b1, const int32_t* __restrict__ offsets,
                     int G, int M_total, int K, int NOUT, __nv_bfloat16* __restrict__ out,
+                    const __nv_bfloat16* __restrict__ xg, int NX, const int32_t* __restrict__ perm,
                     int* __restrict__ status) {
-  constexpr int TN = MODE == 0 ? BN / 2 : BN;  // output columns per tile
+  constexpr bool SWIGLU = MODE != 1;
+  constexpr int TN = SWIGLU ? BN / 2 : BN;  // output columns per tile
+  constexpr int NTHR = kThreads<MODE>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
   // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], done
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-  int* wtot = reinterpret_cast<int*>(tmem_holder + 2);  // [8]
-  int* tile_start = wtot + 8;                            // [G + 1]
+  int* wtot = reinterpret_cast<int*>(tmem_holder + 2);  // [16]
+  int* tile_start = wtot + 16;                           // [G + 1]
 
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int NB = (NOUT + TN - 1) / TN;
@@ -106,7 +124,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
 
   if (t == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full_bar(s), 1);
+      mbar_init(full_bar(s), MODE == 2 ? 1 + 128 : 1);  // TMA arrival (+ one per gather thread)
       mbar_init(empty_bar(s), 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -123,14 +141,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   if (warp == 0 && lane == 0) {
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_a)) : "memory");
+    if (MODE != 2) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_a)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_b0)) : "memory");
-    if (MODE == 0) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_b1)) : "memory");
+    if (SWIGLU) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_b1)) : "memory");
   }
 
   // tile_start[g] = sum over g' < g of (row blocks of g') * NB
   {
-    const int per = (G + THREADS - 1) / THREADS;
+    const int per = (G + NTHR - 1) / NTHR;
     const int g0 = min(G, t * per), g1 = min(G, g0 + per);
     int local = 0;
     for (int g = g0; g < g1; ++g) {
@@ -155,9 +173,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
       const int e = min(max(__ldg(offsets + g + 1), s), M_total);
       base += ((e - s + BM - 1) / BM) * NB;
     }
-    if (t == THREADS - 1) {
+    if (t == NTHR - 1) {
       int tot = 0;
-      for (int w = 0; w < THREADS / 32; ++w) tot += wtot[w];
+      for (int w = 0; w < NTHR / 32; ++w) tot += wtot[w];
       tile_start[G] = tot;
     }
   }
@@ -174,15 +192,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
       uint32_t phase = 0, issued = 0, issued_par = 0;
       for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
         const Tile tl = decode(tile, tile_start, G, offsets, M_total, NB);
-        const int brow = MODE == 0 ? tl.g * NOUT + tl.nb * TN : tl.g * NOUT + tl.nb * TN;
+        const int brow = tl.g * NOUT + tl.nb * TN;
         bool ok = true;
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, status, true)) { ok = false; break; }
           const uint32_t a_dst = smem_u32(smem + stage * STAGE_BYTES);
           const uint32_t b_dst = a_dst + A_BYTES;
-          mbar_expect_tx(full_bar(stage), STAGE_BYTES);
-          tma_load_2d(a_dst, &map_a, kb * BK, tl.row0, full_bar(stage));
-          if (MODE == 0) {
+          mbar_expect_tx(full_bar(stage), MODE == 2 ? B_BYTES : STAGE_BYTES);
+          if (MODE != 2) tma_load_2d(a_dst, &map_a, kb * BK, tl.row0, full_bar(stage));
+          if (SWIGLU) {
             tma_load_2d(b_dst, &map_b0, kb * BK, brow, full_bar(stage));
             tma_load_2d(b_dst + B_BYTES / 2, &map_b1, kb * BK, brow, full_bar(stage));
           } else {
@@ -228,6 +246,75 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
       tc_commit(done_bar);
       mbar_wait(done_bar, 0, abort_flag, status, false);
     }
+  } else if (MODE == 2 && warp >= 6) {
+    // ---------------- A gather (warps 6..9): 32 tile rows per warp ----------------
+    // Copy i of a lane moves 16 bytes (chunk lane % 8) of tile row 32 * w + 4 * i + lane / 8,
+    // so each warp-wide copy reads four whole 128-byte row segments.
+    constexpr int LAG = GATHER_LAG;
+    const int w = warp - 6, c = lane & 7;
+    int stage = 0, pend = 0, oldest = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    // The next tile is decoded, and its token indices loaded, one tile ahead (in two steps,
+    // after this tile's second and third k-blocks) so that a thread never stalls on those
+    // dependent loads while earlier stages still wait for its arrival.
+    Tile tl_next{};
+    int tok_next[8];
+    auto load_tokens = [&]() {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int r = 32 * w + 4 * i + (lane >> 3);
+        tok_next[i] = r < tl_next.rows ? __ldg(perm + tl_next.row0 + r) : -1;
+      }
+    };
+    const int kb_decode = KB > 2 ? 1 : 0, kb_tokens = KB > 2 ? 2 : KB - 1;
+    if (blockIdx.x < total_tiles) {
+      tl_next = decode(blockIdx.x, tile_start, G, offsets, M_total, NB);
+      load_tokens();
+    }
+    for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+      const Tile tl = tl_next;
+      const __nv_bfloat16* src[8];
+      uint32_t live = 0, doff[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int r = 32 * w + 4 * i + (lane >> 3);
+        int tok = tok_next[i];
+        if (r < tl.rows && (unsigned)tok >= (unsigned)NX) {  // not a token of xn: zero row, flagged
+          if (c == 0) atomicOr(status, kStatusBadToken);
+          tok = -1;
+        }
+        src[i] = xg + (size_t)(tok < 0 ? 0 : tok) * K + c * 8;
+        live |= (tok < 0 ? 0u : 1u) << i;  // rows past the group are zero-filled, not read
+        doff[i] = (uint32_t)r * 128u + ((uint32_t)(c ^ (r & 7)) << 4);
+      }
+      const bool more = tile + (int)gridDim.x < total_tiles;
+      for (int kb = 0; kb < KB; ++kb) {
+        if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, status, true)) { ok = false; break; }
+        const uint32_t base = smem_u32(smem + stage * STAGE_BYTES);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) cp_async_16(base + doff[i], src[i] + kb * BK, ((live >> i) & 1u) << 4);
+        cp_async_commit();
+        if (++pend > LAG) {  // the oldest stage's copies are complete once LAG groups remain
+          cp_async_wait<LAG>();
+          fence_proxy_async_smem();
+          mbar_arrive(full_bar(oldest));
+          if (++oldest == STAGES) oldest = 0;
+          --pend;
+        }
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        if (more) {
+          if (kb == kb_decode) tl_next = decode(tile + gridDim.x, tile_start, G, offsets, M_total, NB);
+          if (kb == kb_tokens) load_tokens();
+        }
+      }
+    }
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    for (; pend > 0; --pend) {
+      mbar_arrive(full_bar(oldest));
+      if (++oldest == STAGES) oldest = 0;
+    }
   } else {
     // ---------------- epilogue (warps 2..5) ----------------
     const int q = warp & 3;  // TMEM lane quarter this warp may access
@@ -242,7 +329,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
       const bool valid = row_local < tl.rows;
       __nv_bfloat16* orow = out + (size_t)(tl.row0 + row_local) * NOUT + tl.nb * TN;
-      if (MODE == 0) {
+      if (SWIGLU) {
 #pragma unroll 1
         for (int c = 0; c < TN / 32; ++c) {
           uint32_t gv[32], uv[32];
@@ -327,21 +414,23 @@ bool make_map_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t col
   return r == CUDA_SUCCESS;
 }
 
-size_t smem_bytes(int G) { return 1024 + (size_t)STAGES * STAGE_BYTES + 256 + (size_t)(G + 16) * 4; }
+size_t smem_bytes(int G) { return 1024 + (size_t)STAGES * STAGE_BYTES + 256 + (size_t)(G + 32) * 4; }
 
 template <int MODE>
 moe_status_t launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1, const int32_t* offsets,
-                    int G, int M_total, int K, int NOUT, void* out, int* status, cudaStream_t s) {
+                    int G, int M_total, int K, int NOUT, void* out, int* status, cudaStream_t s,
+                    const void* xg = nullptr, int NX = 0, const int32_t* perm = nullptr) {
   const size_t smem = smem_bytes(G);
   auto kern = grouped_gemm_kernel<MODE>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return MOE_ERR_CUDA;
-  const int TN = MODE == 0 ? BN / 2 : BN;
+  const int TN = MODE != 1 ? BN / 2 : BN;
   const long long NB = (NOUT + TN - 1) / TN;
   const long long max_tiles = ((long long)(M_total + BM - 1) / BM + G) * NB;
   const int grid = (int)std::min<long long>(max_tiles, (long long)sm_count());
-  kern<<<grid, THREADS, smem, s>>>(a, b0, b1, offsets, G, M_total, K, NOUT,
-                                   static_cast<__nv_bfloat16*>(out), status);
+  kern<<<grid, kThreads<MODE>, smem, s>>>(a, b0, b1, offsets, G, M_total, K, NOUT,
+                                          static_cast<__nv_bfloat16*>(out),
+                                          static_cast<const __nv_bfloat16*>(xg), NX, perm, status);
   return launch_status();
 }
 
@@ -437,6 +526,35 @@ extern "C" moe_status_t moe_grouped_swiglu(const void* x_perm, moe_dtype_t dtype
       !tc::make_map_bf16(&md, w_down, (uint64_t)G * D, (uint64_t)F, tc::BN))
     return MOE_ERR_CUDA;
   moe_status_t st = tc::launch<0>(ma, mg, mu, offsets, G, M_total, D, F, h_workspace, status, s);
+  if (st != MOE_OK) return st;
+  return tc::launch<1>(mh, md, md, offsets, G, M_total, F, D, y_perm, status, s);
+}
+
+extern "C" moe_status_t moe_grouped_swiglu_gather(const void* xn, int N, const int32_t* perm_token,
+                                                  const int32_t* offsets, int G, int M_total, int D, int F,
+                                                  const void* w_gate, const void* w_up, const void* w_down,
+                                                  void* h_workspace, void* y_perm, moe_stream_t stream) {
+  using namespace moe;
+  if (G < 1 || M_total < 0 || D <= 0 || F <= 0 || N < 0) return MOE_ERR_INVALID_ARG;
+  if (D % 64 != 0 || F % 64 != 0 || G > tc::MAX_GROUPS) return MOE_ERR_UNSUPPORTED;
+  if ((long long)G * F >= (1LL << 31) || (long long)G * D >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
+  if (M_total == 0) return MOE_OK;
+  if (N == 0) return MOE_ERR_INVALID_ARG;  // rows to gather from, but no tokens
+  if (!xn || !perm_token || !offsets || !w_gate || !w_up || !w_down || !h_workspace || !y_perm)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(xn) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) ||
+      !aligned16(h_workspace) || !aligned16(y_perm))
+    return MOE_ERR_INVALID_ARG;
+  int* status = device_status_word();
+  if (!status) return MOE_ERR_CUDA;
+  cudaStream_t s = as_cuda(stream);
+  CUtensorMap mg, mu, mh, md;
+  if (!tc::make_map_bf16(&mg, w_gate, (uint64_t)G * F, (uint64_t)D, tc::BN / 2) ||
+      !tc::make_map_bf16(&mu, w_up, (uint64_t)G * F, (uint64_t)D, tc::BN / 2) ||
+      !tc::make_map_bf16(&mh, h_workspace, (uint64_t)M_total, (uint64_t)F, tc::BM) ||
+      !tc::make_map_bf16(&md, w_down, (uint64_t)G * D, (uint64_t)F, tc::BN))
+    return MOE_ERR_CUDA;
+  moe_status_t st = tc::launch<2>(mg, mg, mu, offsets, G, M_total, D, F, h_workspace, status, s, xn, N, perm_token);
   if (st != MOE_OK) return st;
   return tc::launch<1>(mh, md, md, offsets, G, M_total, F, D, y_perm, status, s);
 }

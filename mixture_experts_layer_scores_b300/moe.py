@@ -24,7 +24,8 @@ EXPORTS = ("moe_status_string", "moe_last_device_status", "moe_version", "moe_ro
            "moe_permute_workspace_bytes", "moe_permute", "moe_grouped_swiglu",
            "moe_unpermute_combine", "moe_bias_update", "moe_permute_noalloc",
            "moe_permute_noalloc_max_scratch_bytes", "moe_router_split_bytes", "moe_router_split",
-           "moe_router_topk_split", "moe_router_topk_split_workspace_bytes", "moe_permute_capacity")
+           "moe_router_topk_split", "moe_router_topk_split_workspace_bytes", "moe_permute_capacity",
+           "moe_grouped_swiglu_gather")
 
 
 class MoEError(RuntimeError):
@@ -54,6 +55,7 @@ def load():
         "moe_permute_workspace_bytes": ([i32, i32, i32], sz),
         "moe_permute": ([vp, i32, i32, i32, vp, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp], i32),
         "moe_grouped_swiglu": ([vp, i32, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp], i32),
+        "moe_grouped_swiglu_gather": ([vp, i32, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp], i32),
         "moe_unpermute_combine": ([vp, vp, vp, i32, i32, i32, vp, vp, vp, i32, vp], i32),
         "moe_bias_update": ([vp, i32, i64, f32, vp, vp, vp], i32),
         "moe_permute_capacity": ([vp, i32, i32, i32, vp, i32, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp], i32),
@@ -248,6 +250,24 @@ def moe_grouped_swiglu(x_perm, offsets, w_gate, w_up, w_down, h_workspace=None, 
     return y_perm
 
 
+def moe_grouped_swiglu_gather(xn, perm_token, offsets, w_gate, w_up, w_down, h_workspace=None,
+                              y_perm=None, stream=None):
+    """Grouped SwiGLU whose row i reads xn[perm_token[i]] directly (bf16).  Returns y_perm."""
+    L = load()
+    M = perm_token.shape[0]
+    N, D = xn.shape
+    G, F, _ = w_gate.shape
+    if h_workspace is None:
+        h_workspace = torch.empty(M, F, dtype=xn.dtype, device=xn.device)
+    if y_perm is None:
+        y_perm = torch.empty(M, D, dtype=xn.dtype, device=xn.device)
+    _cuda(xn, perm_token, offsets, w_gate, w_up, w_down, h_workspace, y_perm)
+    _chk("moe_grouped_swiglu_gather", L.moe_grouped_swiglu_gather(
+        _p(xn), N, _p(perm_token), _p(offsets), G, M, D, F, _p(w_gate), _p(w_up), _p(w_down),
+        _p(h_workspace), _p(y_perm), _stream(stream)))
+    return y_perm
+
+
 def moe_unpermute_combine(y_perm, row_map, topk_gate, shared_y=None, residual=None, out=None,
                           stream=None):
     """out = residual + shared_y + sum_j gate[:, j] * y_perm[row_map[:, j]]."""
@@ -308,7 +328,10 @@ class MoELayer:
     """Top-k MoE FFN layer forward on one GPU, with reusable device buffers."""
 
     def __init__(self, weights: LayerWeights, N: int, k: int, score_fn="softmax", gamma=1e-3,
-                 dtype=torch.bfloat16, capacity_factor=None):
+                 dtype=torch.bfloat16, capacity_factor=None, gather=False):
+        """gather: (bf16) the first expert GEMM reads its rows from xn through perm_token
+        instead of from a permuted copy, which is then never written.  Off by default: the
+        gathered GEMM costs about as much time as the row copy it removes."""
         w = weights
         self.w, self.k, self.score_fn, self.gamma = w, k, score_fn, gamma
         E = w.w_router.shape[0]
@@ -327,7 +350,8 @@ class MoELayer:
         self.offsets = e(self.E + 1)
         self.row_map = e(N, k)
         self.perm_token = e(R)
-        self.x_perm = e(R, self.D, dt=dtype)
+        self.gather = gather and dtype == torch.bfloat16
+        self.x_perm = None if self.gather else e(R, self.D, dt=dtype)
         self.h_ws = e(R, self.F, dt=dtype)
         self.y_perm = e(R, self.D, dt=dtype)
         self.out = e(N, self.D, dt=dtype)
@@ -349,20 +373,44 @@ class MoELayer:
         """out = h + shared(xn) + sum_j gate_j Expert_j(xn); then the +-gamma bias step."""
         w = self.w
         self.route(xn, stream)
+        self.permute(xn, stream)
+        self.experts(xn, stream)
+        self.shared_expert(xn, stream)
+        self.combine(h, stream)
+        if update_bias:
+            self.bias_step(1, stream)
+        return self.out
+
+    def permute(self, xn, stream=None):
+        """Histogram, scan, stable permutation (and the row copy unless gathering)."""
         moe_permute(xn, self.idx, self.E, self.counts, self.offsets, self.row_map,
-                    self.perm_token, self.x_perm, self.workspace, capacity=self.capacity,
-                    stream=stream)
-        moe_grouped_swiglu(self.x_perm, self.offsets, w.w_gate, w.w_up, w.w_down, self.h_ws,
-                           self.y_perm, stream=stream)
+                    self.perm_token, self.x_perm, self.workspace, copy=not self.gather,
+                    capacity=self.capacity, stream=stream)
+
+    def experts(self, xn, stream=None):
+        """Every routed expert's SwiGLU FFN over its block of permuted rows -> y_perm."""
+        w = self.w
+        if self.gather:
+            moe_grouped_swiglu_gather(xn, self.perm_token, self.offsets, w.w_gate, w.w_up,
+                                      w.w_down, self.h_ws, self.y_perm, stream=stream)
+        else:
+            moe_grouped_swiglu(self.x_perm, self.offsets, w.w_gate, w.w_up, w.w_down, self.h_ws,
+                               self.y_perm, stream=stream)
+
+    def shared_expert(self, xn, stream=None):
+        w = self.w
         if w.shared is not None:
             moe_grouped_swiglu(xn, self.sh_offsets, w.shared[0], w.shared[1], w.shared[2],
                                self.sh_h, self.sh_y, stream=stream)
+
+    def combine(self, h, stream=None):
         moe_unpermute_combine(self.y_perm, self.row_map, self.gate, self.sh_y, h, self.out,
                               stream=stream)
-        if update_bias:
-            moe_bias_update(self.counts, w.bias, self.N * self.k, self.gamma, self.mom,
-                            stream=stream)
-        return self.out
+
+    def bias_step(self, replicas=1, stream=None):
+        """+-gamma step on this step's counts (summed over `replicas` data-parallel copies)."""
+        moe_bias_update(self.counts, self.w.bias, self.N * self.k * replicas, self.gamma,
+                        self.mom, stream=stream)
 
     def route(self, xn, stream=None):
         """Router + top-k.  bf16 activations: the fp32 router weight is re-split into bf16
@@ -380,4 +428,5 @@ class MoELayer:
     @property
     def kernels_per_forward(self):
         router = 3 if self.tc_router else 1
-        return router + 4 + 2 + (2 if self.w.shared else 0) + 1 + 1
+        permute = 3 if self.gather else 4
+        return router + permute + 2 + (2 if self.w.shared else 0) + 1 + 1

@@ -73,6 +73,10 @@ def gpu_layer(cfg, inp, k=None, update_bias=True):
         logits, idx, gate, tie = moe.moe_router_topk(xn, inp["w_router"], bias, k, cfg.score_fn)
     counts, offsets, row_map, perm, x_perm = moe.moe_permute(xn, idx, E)
     y_perm = moe.moe_grouped_swiglu(x_perm, offsets, inp["w_gate"], inp["w_up"], inp["w_down"])
+    y_gather = None
+    if xn.dtype == torch.bfloat16:  # the same GEMM reading its rows through perm_token
+        y_gather = moe.moe_grouped_swiglu_gather(xn, perm, offsets, inp["w_gate"], inp["w_up"],
+                                                 inp["w_down"])
     sh_y = None
     if inp["shared"] is not None:
         off_sh = torch.tensor([0, cfg.N], dtype=torch.int32, device=xn.device)
@@ -86,7 +90,7 @@ def gpu_layer(cfg, inp, k=None, update_bias=True):
     c = lambda t: None if t is None else t.cpu()
     return dict(logits=c(logits), idx=c(idx), gate=c(gate), near_tie=c(tie), counts=c(counts),
                 offsets=c(offsets), row_map=c(row_map), perm_token=c(perm), x_perm=c(x_perm),
-                y_perm=c(y_perm), shared_y=c(sh_y), out=c(out), bias_new=c(bias),
+                y_perm=c(y_perm), y_perm_gather=c(y_gather), shared_y=c(sh_y), out=c(out), bias_new=c(bias),
                 max_over_mean=None if mom is None else float(mom.item()))
 
 

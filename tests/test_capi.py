@@ -72,6 +72,17 @@ def test_host_validation_rejects_before_launch(lib):
     assert lib.moe_grouped_swiglu(vp(16), 1, vp(16), 4, 100, 128, 96, vp(16), vp(16), vp(16), vp(16),
                                   vp(16), None) == -2
     assert lib.moe_grouped_swiglu(None, 1, None, 4, 0, 128, 128, None, None, None, None, None, None) == 0
+    # gathered GEMM: same shape rules; null perm_token; M_total == 0 is a no-op
+    assert lib.moe_grouped_swiglu_gather(vp(16), 50, vp(16), vp(16), 4, 100, 128, 96, vp(16), vp(16),
+                                         vp(16), vp(16), vp(16), None) == -2
+    assert lib.moe_grouped_swiglu_gather(vp(16), 50, None, vp(16), 4, 100, 128, 128, vp(16), vp(16),
+                                         vp(16), vp(16), vp(16), None) == -1
+    assert lib.moe_grouped_swiglu_gather(vp(24), 50, vp(16), vp(16), 4, 100, 128, 128, vp(16), vp(16),
+                                         vp(16), vp(16), vp(16), None) == -1
+    assert lib.moe_grouped_swiglu_gather(vp(16), 0, vp(16), vp(16), 4, 100, 128, 128, vp(16), vp(16),
+                                         vp(16), vp(16), vp(16), None) == -1
+    assert lib.moe_grouped_swiglu_gather(None, 0, None, None, 4, 0, 128, 128, None, None, None, None,
+                                         None, None) == 0
     # combine: k too large; bias: null counts
     assert lib.moe_unpermute_combine(vp(16), vp(16), vp(16), 4, 17, 64, None, None, vp(16), 1, None) == -2
     assert lib.moe_bias_update(None, 8, 64, ctypes.c_float(1e-3), vp(16), None, None) == -1

@@ -3,7 +3,8 @@
 The oracle checks, at each configuration's real size:
 * routing of every token (logits, ids outside the near-tie band, gates);
 * counts, offsets, row map and token permutation, bit for bit;
-* the permuted rows, bit for bit;
+* the permuted rows, bit for bit, and the expert outputs of the row-gathering GEMM against
+  those of the GEMM over the permuted copy, bit for bit;
 * the expert outputs and the layer output of a seeded sample of tokens, computed one expert
   at a time on the CPU from regenerated weights (bf16 tolerance of tests/parity.py);
 * the bias step, bit for bit;
@@ -75,6 +76,14 @@ def test_full_size_layer(name, k):
                                         "perm_token": layer.perm_token.cpu()}, cfg.E, k)
     perm_t = layer.perm_token.long()
     assert torch.equal(layer.x_perm, xn[perm_t])                      # permuted rows exact
+    # the same GEMM reading its rows from xn through perm_token: the same bits
+    w = layer.w
+    y_gather = moe.moe_grouped_swiglu_gather(xn, layer.perm_token, layer.offsets, w.w_gate, w.w_up,
+                                             w.w_down)
+    torch.cuda.synchronize()
+    assert moe.last_device_status() == 0
+    assert torch.equal(y_gather, layer.y_perm)
+    del y_gather
 
     # --- the combine, every token (property) -------------------------------------------
     rm = layer.row_map.long()

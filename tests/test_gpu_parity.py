@@ -50,6 +50,8 @@ def test_layer_parity(name, bias_scale):
     o = P.oracle_layer(cfg, cpu)
     rep = P.compare_layer(cfg, g, o, f32=cfg.dtype == "f32")
     P.moe_delta_close(cfg, g, o, P.np64(cpu["h"]), f32=cfg.dtype == "f32")
+    if g["y_perm_gather"] is not None:  # gathered rows: the same bits as the permuted copy
+        assert torch.equal(g["y_perm_gather"], g["y_perm"])
     print(name, bias_scale, rep)
 
 
@@ -188,6 +190,9 @@ def test_capacity_dropping(factor):
     assert np.array_equal(L.perm_token[:kept].cpu().numpy(), o["perm_token"])
     assert np.array_equal(L.w.bias.cpu().numpy(), o["bias_new"])       # demand drives the bias
     P.assert_close("y_perm (kept rows)", P.np64(L.y_perm[:kept].cpu()), o["y_perm"])
+    y_gather = moe.moe_grouped_swiglu_gather(gi["xn"], L.perm_token, L.offsets, gi["w_gate"], gi["w_up"],
+                                             gi["w_down"])
+    assert torch.equal(y_gather[:kept], L.y_perm[:kept])  # rows gathered from xn: the same bits
     P.assert_close("out", P.np64(out.cpu()), o["out"])
     # a token that lost every slot gets exactly its residual back; tokens that kept every
     # slot get the usual bound on the MoE delta (dropping makes the delta's rms over all
@@ -199,3 +204,25 @@ def test_capacity_dropping(factor):
                   P.np64(ci["h"])[all_kept])
     print("capacity factor", factor, "capacity", cap, "dropped slots", dropped, "of", cfg.N * cfg.k,
           "tokens with no slot kept", int(none_kept.sum()))
+
+
+def test_gather_rejects_bad_token_index():
+    """A permuted row whose token index is outside [0, N) is never read: the gathered GEMM
+    uses a zero row there (SwiGLU(0) = 0, so its output row is exactly 0), every other row is
+    unchanged, and the status word reports MOE_ERR_INVALID_ARG."""
+    cfg = synth.scaled(C["handbook"], N=300, D=256, E=8, F=128, k=2)
+    gi = P.make_inputs(cfg, "cuda")
+    _, idx, _, _ = moe.moe_router_topk_split(gi["xn"], moe.moe_router_split(gi["w_router"]), gi["bias"],
+                                             cfg.k, cfg.score_fn)
+    counts, offsets, row_map, perm, x_perm = moe.moe_permute(gi["xn"], idx, cfg.E)
+    y_ref = moe.moe_grouped_swiglu(x_perm, offsets, gi["w_gate"], gi["w_up"], gi["w_down"])
+    bad = perm.clone()
+    bad[5], bad[400] = cfg.N + 7, -3
+    y = moe.moe_grouped_swiglu_gather(gi["xn"], bad, offsets, gi["w_gate"], gi["w_up"], gi["w_down"])
+    torch.cuda.synchronize()
+    assert moe.STATUS[moe.last_device_status()] == "MOE_ERR_INVALID_ARG"
+    keep = torch.ones(perm.shape[0], dtype=torch.bool, device="cuda")
+    keep[5] = keep[400] = False
+    assert torch.equal(y[keep], y_ref[keep])
+    assert not y[~keep].any()
+    assert moe.last_device_status() == 0  # reading the status clears it
