@@ -222,7 +222,11 @@ moe_status_t moe_permute_noalloc(const void* xn, moe_dtype_t dtype, int N, int D
  *   h_workspace [M_total, F]  scratch for H = SiLU(x W_gate^T) * (x W_up^T)
  *   y_perm      [M_total, D]  out: H W_down^T per row (rows past offsets[G] untouched)
  * MOE_BF16: tcgen05 tensor-core kernels, fp32 accumulation in tensor memory, H and Y
- *           rounded to bf16.  MOE_F32: CUDA-core fp32 kernels.
+ *           rounded to bf16.  When the groups average at least 256 rows, two-CTA
+ *           clusters share each 256-row tile (tcgen05 cta_group::2); otherwise one CTA
+ *           per 128-row tile.  Both give the same bits.  The environment variable
+ *           MOE_GROUPED_GEMM=pair or =single forces one of the two (read on every call).
+ *           MOE_F32: CUDA-core fp32 kernels.
  * Requires D % 64 == 0, F % 64 == 0, 1 <= G.
  */
 moe_status_t moe_grouped_swiglu(const void* x_perm, moe_dtype_t dtype, const int32_t* offsets,

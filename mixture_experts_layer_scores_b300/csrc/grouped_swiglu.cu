@@ -25,6 +25,8 @@
 //
 // fp32 path: plain CUDA-core kernels (one thread per output element).
 #include <algorithm>
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "tc_common.cuh"
@@ -83,11 +85,13 @@ __device__ __forceinline__ Tile decode(int tile, const int* tile_start, int G, c
 //         Warps 6..9 copy 32 tile rows each with 16-byte cp.async into the 128-byte-swizzled
 //         K-major layout the MMA descriptors expect; each thread keeps LAG k-blocks of copies
 //         in flight, then waits for the oldest, fences the async proxy and arrives on that
-//         stage's full barrier (initialised for 1 + 128 arrivals).  Warp 0 loads only B.
+//         stage's full barrier (initialised for 1 + 128 arrivals).
 //         LAG <= STAGES - 2 keeps one k-block queued on the tensor pipe while a stage fills:
 //         the arrival for stage s needs the MMA of stage s + LAG - STAGES to have completed.
+// Warp 6 (MODE 0/1) issues the A-tile copies while warp 0 issues the B-tile copies: one
+// thread issuing every copy of a stage leaves the copy engine underused (measured).
 template <int MODE>
-constexpr int kThreads = MODE == 2 ? THREADS + 128 : THREADS;
+constexpr int kThreads = MODE == 2 ? THREADS + 128 : THREADS + 32;
 #ifndef MOE_GATHER_LAG
 #define MOE_GATHER_LAG (STAGES - 2)
 #endif
@@ -100,7 +104,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
                     const __grid_constant__ CUtensorMap map_b1, const int32_t* __restrict__ offsets,
                     int G, int M_total, int K, int NOUT, __nv_bfloat16* __restrict__ out,
                     const __nv_bfloat16* __restrict__ xg, int NX, const int32_t* __restrict__ perm,
-                    int* __restrict__ status) {
+                    int b_planes, int* __restrict__ status) {
   constexpr bool SWIGLU = MODE != 1;
   constexpr int TN = SWIGLU ? BN / 2 : BN;  // output columns per tile
   constexpr int NTHR = kThreads<MODE>;
@@ -124,7 +128,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
 
   if (t == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full_bar(s), MODE == 2 ? 1 + 128 : 1);  // TMA arrival (+ one per gather thread)
+      mbar_init(full_bar(s), MODE == 2 ? 1 + 128 : 2);  // B copies + A copies (or one per gather thread)
       mbar_init(empty_bar(s), 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -140,8 +144,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
                  "r"(TMEM_COLS));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
+  if (warp == 6 && lane == 0 && MODE != 2)
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_a)) : "memory");
   if (warp == 0 && lane == 0) {
-    if (MODE != 2) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_a)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_b0)) : "memory");
     if (SWIGLU) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_b1)) : "memory");
   }
@@ -187,7 +192,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
 
   if (warp == 0) {
     if (lane == 0) {
-      // ---------------- TMA producer ----------------
+      // ---------------- TMA producer: weight (B) tiles ----------------
       int stage = 0;
       uint32_t phase = 0, issued = 0, issued_par = 0;
       for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
@@ -198,9 +203,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, status, true)) { ok = false; break; }
           const uint32_t a_dst = smem_u32(smem + stage * STAGE_BYTES);
           const uint32_t b_dst = a_dst + A_BYTES;
-          mbar_expect_tx(full_bar(stage), MODE == 2 ? B_BYTES : STAGE_BYTES);
-          if (MODE != 2) tma_load_2d(a_dst, &map_a, kb * BK, tl.row0, full_bar(stage));
-          if (SWIGLU) {
+          mbar_expect_tx(full_bar(stage), B_BYTES);
+          if (SWIGLU && b_planes != 0) {  // gate and up rows as the two planes of one box
+            tma_load_3d(b_dst, &map_b0, kb * BK, brow, 0, full_bar(stage));
+          } else if (SWIGLU) {
             tma_load_2d(b_dst, &map_b0, kb * BK, brow, full_bar(stage));
             tma_load_2d(b_dst + B_BYTES / 2, &map_b1, kb * BK, brow, full_bar(stage));
           } else {
@@ -245,6 +251,27 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
       // every MMA issued so far completes before TMEM is freed
       tc_commit(done_bar);
       mbar_wait(done_bar, 0, abort_flag, status, false);
+    }
+  } else if (MODE != 2 && warp == 6) {
+    if (lane == 0) {
+      // ---------------- TMA producer: activation (A) tiles ----------------
+      int stage = 0;
+      uint32_t phase = 0, issued = 0, issued_par = 0;
+      for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+        const Tile tl = decode(tile, tile_start, G, offsets, M_total, NB);
+        bool ok = true;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, status, true)) { ok = false; break; }
+          mbar_expect_tx(full_bar(stage), A_BYTES);
+          tma_load_2d(smem_u32(smem + stage * STAGE_BYTES), &map_a, kb * BK, tl.row0, full_bar(stage));
+          issued |= 1u << stage;
+          issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+      }
+      for (int s = 0; s < STAGES; ++s)
+        if ((issued >> s) & 1u) mbar_wait(full_bar(s), (issued_par >> s) & 1u, abort_flag, status, false);
     }
   } else if (MODE == 2 && warp >= 6) {
     // ---------------- A gather (warps 6..9): 32 tile rows per warp ----------------
@@ -333,8 +360,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
 #pragma unroll 1
         for (int c = 0; c < TN / 32; ++c) {
           uint32_t gv[32], uv[32];
-          tmem_ld32(taddr + c * 32, gv);
-          tmem_ld32(taddr + TN + c * 32, uv);
+          const uint32_t gcol = b_planes == 2 ? TN : 0;  // up rows came first in B
+          tmem_ld32(taddr + gcol + c * 32, gv);
+          tmem_ld32(taddr + (TN - gcol) + c * 32, uv);
           tmem_ld_wait();
           if (valid && tl.nb * TN + c * 32 < NOUT) {
             uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
@@ -345,7 +373,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
               for (int i = 0; i < 8; ++i) {
                 const float g = __uint_as_float(gv[v * 8 + i]);
                 const float u = __uint_as_float(uv[v * 8 + i]);
-                h[i] = (g / (1.0f + __expf(-g))) * u;
+                h[i] = __fdividef(g, 1.0f + __expf(-g)) * u;
               }
               dst[v] = f32_to_bf16x8(h);
             }
@@ -385,6 +413,256 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
   }
 }
 
+// ---- CTA-pair kernel -------------------------------------------------------------------
+// A cluster of two CTAs computes a 256-row x 256-column tile with tcgen05.mma.cta_group::2:
+// each CTA holds its own 128 rows of A and half of the B rows (GEMM1: the leader the gate
+// rows, the other CTA the up rows of the same 128 outputs; GEMM2: 128 rows of W_down each),
+// so each SM stages 32 KB per 64-wide k-block instead of 48 KB, and six stages fit.  Each CTA
+// issues its A copies from warp 6 and its B copies from warp 0 (two issuing warps keep the
+// copy engine busier than one, measured); all copies count on the leader's full barrier.
+// The leader's warp 1 issues every MMA and releases a stage in both CTAs with one multicast
+// commit; each CTA's epilogue warps drain their own 128 TMEM lanes and arrive on the
+// leader's accumulator-empty barrier.
+namespace pair {
+constexpr int PM = 256;                  // rows per pair tile
+constexpr int HB = 128;                  // B rows per CTA
+constexpr int STAGES = 6;
+constexpr int A_BYTES = BM * BK * 2;     // 16 KB
+constexpr int B_BYTES = HB * BK * 2;     // 16 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int THREADS = 224;             // warps: 0 B copies, 1 MMA, 2-5 epilogue, 6 A copies
+constexpr uint32_t IDESC = idesc_bf16(PM, BN);
+}  // namespace pair
+
+template <int MODE>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::THREADS, 1)
+pair_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b0,
+                 const __grid_constant__ CUtensorMap map_b1, const int32_t* __restrict__ offsets,
+                 int G, int M_total, int K, int NOUT, __nv_bfloat16* __restrict__ out, int* __restrict__ status) {
+  constexpr bool SWIGLU = MODE == 0;
+  constexpr int TN = SWIGLU ? BN / 2 : BN;  // output columns per tile
+  constexpr int S = pair::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * pair::STAGE_BYTES);
+  // bars: full[S] (leader's are used), empty[S], tfull[2], tempty[2] (leader's), done
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  int* wtot = reinterpret_cast<int*>(tmem_holder + 2);  // [8]
+  int* tile_start = wtot + 8;                            // [G + 1]
+
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const uint32_t rank = cluster_rank();
+  const bool leader = rank == 0;
+  const int pair_id = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+  const int NB = (NOUT + TN - 1) / TN;
+  const int KB = K / BK;
+  auto full_bar = [&](int s) { return smem_u32(bars + s); };
+  auto empty_bar = [&](int s) { return smem_u32(bars + S + s); };
+  auto tfull_bar = [&](int a) { return smem_u32(bars + 2 * S + a); };
+  auto tempty_bar = [&](int a) { return smem_u32(bars + 2 * S + 2 + a); };
+  const uint32_t done_bar = smem_u32(bars + 2 * S + 4);
+
+  if (t == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full_bar(s), 2);   // the leader's two copy-issuing threads; bytes of both CTAs
+      mbar_init(empty_bar(s), 1);  // one multicast commit per use
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 8);  // four epilogue warps in each CTA of the pair
+    }
+    mbar_init(done_bar, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {  // warp 1 of both CTAs allocates the pair's tensor memory together
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_holder)),
+                 "r"(TMEM_COLS));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
+  }
+  if (warp == 0 && lane == 0) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_b0)) : "memory");
+    if (SWIGLU) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_b1)) : "memory");
+  }
+  if (warp == 6 && lane == 0)
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_a)) : "memory");
+
+  // tile_start[g] = sum over g' < g of (256-row blocks of g') * NB
+  {
+    const int per = (G + pair::THREADS - 1) / pair::THREADS;
+    const int g0 = min(G, t * per), g1 = min(G, g0 + per);
+    int local = 0;
+    for (int g = g0; g < g1; ++g) {
+      const int s0 = min(max(__ldg(offsets + g), 0), M_total);
+      const int e0 = min(max(__ldg(offsets + g + 1), s0), M_total);
+      local += ((e0 - s0 + pair::PM - 1) / pair::PM) * NB;
+    }
+    int incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += y;
+    }
+    if (lane == 31) wtot[warp] = incl;
+    __syncthreads();
+    int base = 0;
+    for (int w = 0; w < warp; ++w) base += wtot[w];
+    base += incl - local;
+    for (int g = g0; g < g1; ++g) {
+      tile_start[g] = base;
+      const int s0 = min(max(__ldg(offsets + g), 0), M_total);
+      const int e0 = min(max(__ldg(offsets + g + 1), s0), M_total);
+      base += ((e0 - s0 + pair::PM - 1) / pair::PM) * NB;
+    }
+    if (t == pair::THREADS - 1) {
+      int tot = 0;
+      for (int w = 0; w < pair::THREADS / 32; ++w) tot += wtot[w];
+      tile_start[G] = tot;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers and tensor memory exist before any cross-CTA use
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  const int total_tiles = tile_start[G];
+
+  if ((warp == 0 || warp == 6) && lane == 0) {
+    // ---------------- copy issue: warp 0 the B half, warp 6 the A rows ----------------
+    const bool is_b = warp == 0;
+    int stage = 0;
+    uint32_t phase = 0, issued = 0, issued_par = 0;
+    for (int tile = pair_id; tile < total_tiles; tile += npairs) {
+      const Tile tl = decode_rows<pair::PM>(tile, tile_start, G, offsets, M_total, NB);
+      const int a_row = tl.row0 + (int)rank * BM;
+      const int b_row = SWIGLU ? tl.g * NOUT + tl.nb * TN : tl.g * NOUT + tl.nb * TN + (int)rank * pair::HB;
+      const CUtensorMap* mb = (SWIGLU && !leader) ? &map_b1 : &map_b0;
+      bool ok = true;
+      for (int kb = 0; kb < KB; ++kb) {
+        if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, status, true)) { ok = false; break; }
+        const uint32_t dst = smem_u32(smem + stage * pair::STAGE_BYTES) + (is_b ? pair::A_BYTES : 0);
+        const uint32_t lead_full = map_to_rank(full_bar(stage), 0);
+        if (leader) mbar_expect_tx(full_bar(stage), 2 * (is_b ? pair::B_BYTES : pair::A_BYTES));
+        if (is_b) tma_load_2d_pair(dst, mb, kb * BK, b_row, lead_full);
+        else tma_load_2d_pair(dst, &map_a, kb * BK, a_row, lead_full);
+        issued |= 1u << stage;
+        issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+        if (++stage == S) { stage = 0; phase ^= 1u; }
+      }
+      if (!ok) break;
+    }
+    // every copy this thread issued has landed once the leader's MMA has released its stage
+    for (int s = 0; s < S; ++s)
+      if ((issued >> s) & 1u) mbar_wait(empty_bar(s), (issued_par >> s) & 1u, abort_flag, status, false);
+  } else if (warp == 1) {
+    if (lane == 0) {
+      if (leader) {
+        // ---------------- MMA issue (leader only) ----------------
+        int stage = 0, acc = 0;
+        uint32_t phase = 0, acc_phase = 0;
+        for (int tile = pair_id; tile < total_tiles; tile += npairs) {
+          if (!mbar_wait_cluster(tempty_bar(acc), acc_phase ^ 1u, abort_flag, status, true)) break;
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+          bool ok = true;
+          for (int kb = 0; kb < KB; ++kb) {
+            if (!mbar_wait(full_bar(stage), phase, abort_flag, status, true)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t a_base = smem_u32(smem + stage * pair::STAGE_BYTES);
+            const uint32_t b_base = a_base + pair::A_BYTES;
+#pragma unroll
+            for (int k = 0; k < BK / UK; ++k)
+              tc_mma_pair(d_tmem, sw128_desc(a_base + k * UK * 2), sw128_desc(b_base + k * UK * 2), pair::IDESC,
+                          (kb | k) != 0 ? 1u : 0u);
+            tc_commit_pair(empty_bar(stage), 0x3);
+            if (++stage == S) { stage = 0; phase ^= 1u; }
+          }
+          if (!ok) break;
+          tc_commit_pair(tfull_bar(acc), 0x3);
+          if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        }
+        // every pair MMA issued so far completes before either CTA frees its tensor memory
+        tc_commit_pair(done_bar, 0x3);
+      }
+      mbar_wait(done_bar, 0, abort_flag, status, false);
+    }
+  } else if (warp >= 2 && warp <= 5) {
+    // ---------------- epilogue (warps 2..5 of both CTAs) ----------------
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int row_local = q * 32 + lane;
+    const uint32_t lead_tempty0 = map_to_rank(tempty_bar(0), 0), lead_tempty1 = map_to_rank(tempty_bar(1), 0);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = pair_id; tile < total_tiles; tile += npairs) {
+      const Tile tl = decode_rows<pair::PM>(tile, tile_start, G, offsets, M_total, NB);
+      const bool ok = mbar_wait(tfull_bar(acc), acc_phase, abort_flag, status, true);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+      const int pr = (int)rank * BM + row_local;  // row within the pair tile
+      const bool valid = pr < tl.rows;
+      __nv_bfloat16* orow = out + (size_t)(tl.row0 + pr) * NOUT + tl.nb * TN;
+      if (SWIGLU) {
+#pragma unroll 1
+        for (int c = 0; c < TN / 32; ++c) {
+          uint32_t gv[32], uv[32];
+          tmem_ld32(taddr + c * 32, gv);
+          tmem_ld32(taddr + TN + c * 32, uv);
+          tmem_ld_wait();
+          if (valid && tl.nb * TN + c * 32 < NOUT) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              float h[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const float g = __uint_as_float(gv[v * 8 + i]);
+                const float u = __uint_as_float(uv[v * 8 + i]);
+                h[i] = __fdividef(g, 1.0f + __expf(-g)) * u;
+              }
+              dst[v] = f32_to_bf16x8(h);
+            }
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < TN / 32; ++c) {
+          uint32_t yv[32];
+          tmem_ld32(taddr + c * 32, yv);
+          tmem_ld_wait();
+          if (valid && tl.nb * TN + c * 32 < NOUT) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              float y[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) y[i] = __uint_as_float(yv[v * 8 + i]);
+              dst[v] = f32_to_bf16x8(y);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (leader) mbar_arrive(tempty_bar(acc));
+        else mbar_arrive_remote(acc == 0 ? lead_tempty0 : lead_tempty1);
+      }
+      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // neither CTA frees tensor memory or exits while the pair still works
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS));
+  }
+}
+
 // ---- host: tensor maps ---------------------------------------------------------------
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -414,12 +692,35 @@ bool make_map_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t col
   return r == CUDA_SUCCESS;
 }
 
+// One tensor map over both projections: planes {gate, up} (or {up, gate} when w_up lies
+// below w_gate; *planes = 2) 'plane distance' bytes apart, so that a 3-D box of
+// (64 columns, box_rows rows, 2 planes) brings the gate and up rows of a tile in one copy.
+// Returns false (and the caller keeps two 2-D maps) if the driver rejects the layout.
+bool make_map_gate_up(CUtensorMap* m, const void* w_gate, const void* w_up, uint64_t rows, uint64_t cols,
+                      uint32_t box_rows, int* planes) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const uintptr_t g = reinterpret_cast<uintptr_t>(w_gate), u = reinterpret_cast<uintptr_t>(w_up);
+  const uintptr_t lo = g < u ? g : u, dist = g < u ? u - g : g - u;
+  if (dist < rows * cols * 2 || dist % 16 != 0 || dist >= (1ULL << 40)) return false;
+  cuuint64_t dims[3] = {cols, rows, 2};
+  cuuint64_t strides[2] = {cols * 2, (cuuint64_t)dist};
+  cuuint32_t box[3] = {(cuuint32_t)BK, box_rows, 2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, reinterpret_cast<void*>(lo), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return false;
+  *planes = g < u ? 1 : 2;
+  return true;
+}
+
 size_t smem_bytes(int G) { return 1024 + (size_t)STAGES * STAGE_BYTES + 256 + (size_t)(G + 32) * 4; }
 
 template <int MODE>
 moe_status_t launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1, const int32_t* offsets,
                     int G, int M_total, int K, int NOUT, void* out, int* status, cudaStream_t s,
-                    const void* xg = nullptr, int NX = 0, const int32_t* perm = nullptr) {
+                    const void* xg = nullptr, int NX = 0, const int32_t* perm = nullptr, int b_planes = 0) {
   const size_t smem = smem_bytes(G);
   auto kern = grouped_gemm_kernel<MODE>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
@@ -430,7 +731,25 @@ moe_status_t launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorM
   const int grid = (int)std::min<long long>(max_tiles, (long long)sm_count());
   kern<<<grid, kThreads<MODE>, smem, s>>>(a, b0, b1, offsets, G, M_total, K, NOUT,
                                           static_cast<__nv_bfloat16*>(out),
-                                          static_cast<const __nv_bfloat16*>(xg), NX, perm, status);
+                                          static_cast<const __nv_bfloat16*>(xg), NX, perm, b_planes, status);
+  return launch_status();
+}
+
+size_t pair_smem_bytes(int G) { return 1024 + (size_t)pair::STAGES * pair::STAGE_BYTES + 256 + (size_t)(G + 16) * 4; }
+
+template <int MODE>
+moe_status_t launch_pair(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1, const int32_t* offsets,
+                         int G, int M_total, int K, int NOUT, void* out, int* status, cudaStream_t s) {
+  const size_t smem = pair_smem_bytes(G);
+  auto kern = pair_gemm_kernel<MODE>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  const int TN = MODE == 0 ? BN / 2 : BN;
+  const long long NB = (NOUT + TN - 1) / TN;
+  const long long max_tiles = ((long long)(M_total + pair::PM - 1) / pair::PM + G) * NB;
+  const int pairs = (int)std::min<long long>(max_tiles, (long long)(sm_count() / 2));
+  kern<<<2 * pairs, pair::THREADS, smem, s>>>(a, b0, b1, offsets, G, M_total, K, NOUT,
+                                              static_cast<__nv_bfloat16*>(out), status);
   return launch_status();
 }
 
@@ -489,6 +808,20 @@ __global__ void swiglu_down_kernel(const float* __restrict__ h, const int32_t* _
 }  // namespace simt
 }  // namespace moe
 
+namespace moe {
+namespace tc {
+// CTA-pair tiles (256 rows) pay off when experts average at least two 128-row blocks; the
+// MOE_GROUPED_GEMM environment variable ("pair", "single", anything else = automatic)
+// overrides the choice.
+bool use_pair(int G, int M_total) {
+  const char* e = std::getenv("MOE_GROUPED_GEMM");
+  if (e && std::strcmp(e, "pair") == 0) return true;
+  if (e && std::strcmp(e, "single") == 0) return false;
+  return (long long)M_total >= 256LL * G;
+}
+}  // namespace tc
+}  // namespace moe
+
 extern "C" moe_status_t moe_grouped_swiglu(const void* x_perm, moe_dtype_t dtype, const int32_t* offsets,
                                            int G, int M_total, int D, int F, const void* w_gate,
                                            const void* w_up, const void* w_down, void* h_workspace,
@@ -518,6 +851,18 @@ extern "C" moe_status_t moe_grouped_swiglu(const void* x_perm, moe_dtype_t dtype
   }
   int* status = device_status_word();
   if (!status) return MOE_ERR_CUDA;
+  if (tc::use_pair(G, M_total)) {
+    CUtensorMap ma, mg, mu, mh, md;
+    if (!tc::make_map_bf16(&ma, x_perm, (uint64_t)M_total, (uint64_t)D, tc::BM) ||
+        !tc::make_map_bf16(&mg, w_gate, (uint64_t)G * F, (uint64_t)D, tc::pair::HB) ||
+        !tc::make_map_bf16(&mu, w_up, (uint64_t)G * F, (uint64_t)D, tc::pair::HB) ||
+        !tc::make_map_bf16(&mh, h_workspace, (uint64_t)M_total, (uint64_t)F, tc::BM) ||
+        !tc::make_map_bf16(&md, w_down, (uint64_t)G * D, (uint64_t)F, tc::pair::HB))
+      return MOE_ERR_CUDA;
+    moe_status_t st = tc::launch_pair<0>(ma, mg, mu, offsets, G, M_total, D, F, h_workspace, status, s);
+    if (st != MOE_OK) return st;
+    return tc::launch_pair<1>(mh, md, md, offsets, G, M_total, F, D, y_perm, status, s);
+  }
   CUtensorMap ma, mg, mu, mh, md;
   if (!tc::make_map_bf16(&ma, x_perm, (uint64_t)M_total, (uint64_t)D, tc::BM) ||
       !tc::make_map_bf16(&mg, w_gate, (uint64_t)G * F, (uint64_t)D, tc::BN / 2) ||
@@ -525,7 +870,12 @@ extern "C" moe_status_t moe_grouped_swiglu(const void* x_perm, moe_dtype_t dtype
       !tc::make_map_bf16(&mh, h_workspace, (uint64_t)M_total, (uint64_t)F, tc::BM) ||
       !tc::make_map_bf16(&md, w_down, (uint64_t)G * D, (uint64_t)F, tc::BN))
     return MOE_ERR_CUDA;
-  moe_status_t st = tc::launch<0>(ma, mg, mu, offsets, G, M_total, D, F, h_workspace, status, s);
+  CUtensorMap mgu;
+  int planes = 0;
+  const bool gu = tc::make_map_gate_up(&mgu, w_gate, w_up, (uint64_t)G * F, (uint64_t)D, tc::BN / 2, &planes);
+  moe_status_t st = gu ? tc::launch<0>(ma, mgu, mgu, offsets, G, M_total, D, F, h_workspace, status, s, nullptr, 0,
+                                       nullptr, planes)
+                       : tc::launch<0>(ma, mg, mu, offsets, G, M_total, D, F, h_workspace, status, s);
   if (st != MOE_OK) return st;
   return tc::launch<1>(mh, md, md, offsets, G, M_total, F, D, y_perm, status, s);
 }
@@ -554,7 +904,13 @@ extern "C" moe_status_t moe_grouped_swiglu_gather(const void* xn, int N, const i
       !tc::make_map_bf16(&mh, h_workspace, (uint64_t)M_total, (uint64_t)F, tc::BM) ||
       !tc::make_map_bf16(&md, w_down, (uint64_t)G * D, (uint64_t)F, tc::BN))
     return MOE_ERR_CUDA;
-  moe_status_t st = tc::launch<2>(mg, mg, mu, offsets, G, M_total, D, F, h_workspace, status, s, xn, N, perm_token);
+  CUtensorMap mgu;
+  int planes = 0;
+  const bool gu = tc::make_map_gate_up(&mgu, w_gate, w_up, (uint64_t)G * F, (uint64_t)D, tc::BN / 2, &planes);
+  moe_status_t st = gu ? tc::launch<2>(mgu, mgu, mgu, offsets, G, M_total, D, F, h_workspace, status, s, xn, N,
+                                       perm_token, planes)
+                       : tc::launch<2>(mg, mg, mu, offsets, G, M_total, D, F, h_workspace, status, s, xn, N,
+                                       perm_token);
   if (st != MOE_OK) return st;
   return tc::launch<1>(mh, md, md, offsets, G, M_total, F, D, y_perm, status, s);
 }

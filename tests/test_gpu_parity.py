@@ -226,3 +226,29 @@ def test_gather_rejects_bad_token_index():
     assert torch.equal(y[keep], y_ref[keep])
     assert not y[~keep].any()
     assert moe.last_device_status() == 0  # reading the status clears it
+
+
+PAIR_CASES = {
+    # experts of 150..1200 rows: full 256-row pair tiles, ragged last tiles, 128-column tails
+    "pair_ragged_F384": synth.scaled(C["handbook"], N=1500, D=256, E=4, F=384, k=2),
+    "pair_E8_k2": synth.scaled(C["mixtral"], N=1024, D=512, E=8, F=256, k=2),
+    "pair_with_empty_experts": synth.scaled(C["skewed"], N=2048, D=256, E=16, F=128, k=2),
+}
+
+
+@pytest.mark.parametrize("name", list(PAIR_CASES))
+def test_grouped_gemm_pair_and_single_agree(name, monkeypatch):
+    """The CTA-pair grouped GEMM (256-row tiles over two SMs) and the single-CTA one give the
+    same bits on the same permuted rows, and the layer matches the oracle with either."""
+    cfg = PAIR_CASES[name]
+    cpu = P.make_inputs(cfg, "cpu")
+    o = P.oracle_layer(cfg, cpu)
+    got = {}
+    for variant in ("pair", "single"):
+        monkeypatch.setenv("MOE_GROUPED_GEMM", variant)
+        g = P.gpu_layer(cfg, P.make_inputs(cfg, "cuda"))
+        P.compare_layer(cfg, g, o)
+        P.moe_delta_close(cfg, g, o, P.np64(cpu["h"]))
+        got[variant] = g
+    assert torch.equal(got["pair"]["y_perm"], got["single"]["y_perm"])
+    assert torch.equal(got["pair"]["out"], got["single"]["out"])
