@@ -415,30 +415,40 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
 
 // ---- CTA-pair kernel -------------------------------------------------------------------
 // A cluster of two CTAs computes a 256-row x 256-column tile with tcgen05.mma.cta_group::2:
-// each CTA holds its own 128 rows of A and half of the B rows (GEMM1: the leader the gate
-// rows, the other CTA the up rows of the same 128 outputs; GEMM2: 128 rows of W_down each),
-// so each SM stages 32 KB per 64-wide k-block instead of 48 KB, and six stages fit.  Each CTA
-// issues its A copies from warp 6 and its B copies from warp 0 (two issuing warps keep the
-// copy engine busier than one, measured); all copies count on the leader's full barrier.
-// The leader's warp 1 issues every MMA and releases a stage in both CTAs with one multicast
-// commit; each CTA's epilogue warps drain their own 128 TMEM lanes and arrive on the
-// leader's accumulator-empty barrier.
+// each CTA holds its own 128 rows of A and half of the B rows, so each SM stages 32 KB per
+// 64-wide k-block instead of 48 KB, and six stages fit.  The last rows of an expert, when
+// 128 or fewer, form a half tile: an M = 128 pair MMA over 64 rows per CTA (measured TMEM
+// layout: a CTA's 64 rows sit in lanes 0-63 for accumulator columns 0-127 and again in
+// lanes 64-127 for columns 128-255), so no expert wastes more than 127 padded rows.
+// GEMM1's B half of each CTA is [64 gate rows; the same 64 up rows] (one two-plane box), so
+// every lane holds the gate and up values of the same outputs.  Each CTA issues its A
+// copies from warp 6 and its B copies from warp 0 (two issuing warps keep the copy engine
+// busier than one, measured); all copies count on the leader's full barrier.  The leader's
+// warp 1 issues every MMA and releases a stage in both CTAs with one multicast commit; each
+// CTA's epilogue warps drain their own TMEM lanes and arrive on the leader's
+// accumulator-empty barrier.
 namespace pair {
 constexpr int PM = 256;                  // rows per pair tile
 constexpr int HB = 128;                  // B rows per CTA
 constexpr int STAGES = 6;
-constexpr int A_BYTES = BM * BK * 2;     // 16 KB
+constexpr int A_BYTES = BM * BK * 2;     // 16 KB (8 KB used by a half tile)
 constexpr int B_BYTES = HB * BK * 2;     // 16 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int THREADS = 224;             // warps: 0 B copies, 1 MMA, 2-5 epilogue, 6 A copies
-constexpr uint32_t IDESC = idesc_bf16(PM, BN);
+constexpr uint32_t IDESC_FULL = idesc_bf16(PM, BN);
+constexpr uint32_t IDESC_HALF = idesc_bf16(PM / 2, BN);
 }  // namespace pair
 
+// map_a / map_a_half: A with 128-row / 64-row boxes.  MODE 0: map_b is a two-plane gate/up
+// map with a (64, 64, 2) box (b_planes 1: gate plane first, 2: up plane first) or, with
+// b_planes 0, a 64-row gate map with map_b_up the matching up map.  MODE 1: map_b is W_down
+// with a 128-row box.
 template <int MODE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::THREADS, 1)
-pair_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b0,
-                 const __grid_constant__ CUtensorMap map_b1, const int32_t* __restrict__ offsets,
-                 int G, int M_total, int K, int NOUT, __nv_bfloat16* __restrict__ out, int* __restrict__ status) {
+pair_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_a_half,
+                 const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUtensorMap map_b_up,
+                 const int32_t* __restrict__ offsets, int G, int M_total, int K, int NOUT, int b_planes,
+                 __nv_bfloat16* __restrict__ out, int* __restrict__ status) {
   constexpr bool SWIGLU = MODE == 0;
   constexpr int TN = SWIGLU ? BN / 2 : BN;  // output columns per tile
   constexpr int S = pair::STAGES;
@@ -482,11 +492,14 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
   }
   if (warp == 0 && lane == 0) {
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_b0)) : "memory");
-    if (SWIGLU) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_b1)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_b)) : "memory");
+    if (SWIGLU && b_planes == 0)
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_b_up)) : "memory");
   }
-  if (warp == 6 && lane == 0)
+  if (warp == 6 && lane == 0) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_a)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_a_half)) : "memory");
+  }
 
   // tile_start[g] = sum over g' < g of (256-row blocks of g') * NB
   {
@@ -535,17 +548,26 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
     uint32_t phase = 0, issued = 0, issued_par = 0;
     for (int tile = pair_id; tile < total_tiles; tile += npairs) {
       const Tile tl = decode_rows<pair::PM>(tile, tile_start, G, offsets, M_total, NB);
-      const int a_row = tl.row0 + (int)rank * BM;
-      const int b_row = SWIGLU ? tl.g * NOUT + tl.nb * TN : tl.g * NOUT + tl.nb * TN + (int)rank * pair::HB;
-      const CUtensorMap* mb = (SWIGLU && !leader) ? &map_b1 : &map_b0;
+      const bool half = tl.rows <= pair::PM / 2;
+      const int a_row = tl.row0 + (int)rank * (half ? BM / 2 : BM);
+      const int b_row = tl.g * NOUT + tl.nb * TN + (int)rank * (SWIGLU ? TN / 2 : pair::HB);
+      const uint32_t tx = is_b ? 2 * pair::B_BYTES : 2 * (half ? pair::A_BYTES / 2 : pair::A_BYTES);
       bool ok = true;
       for (int kb = 0; kb < KB; ++kb) {
         if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, status, true)) { ok = false; break; }
         const uint32_t dst = smem_u32(smem + stage * pair::STAGE_BYTES) + (is_b ? pair::A_BYTES : 0);
         const uint32_t lead_full = map_to_rank(full_bar(stage), 0);
-        if (leader) mbar_expect_tx(full_bar(stage), 2 * (is_b ? pair::B_BYTES : pair::A_BYTES));
-        if (is_b) tma_load_2d_pair(dst, mb, kb * BK, b_row, lead_full);
-        else tma_load_2d_pair(dst, &map_a, kb * BK, a_row, lead_full);
+        if (leader) mbar_expect_tx(full_bar(stage), tx);
+        if (!is_b) {
+          tma_load_2d_pair(dst, half ? &map_a_half : &map_a, kb * BK, a_row, lead_full);
+        } else if (SWIGLU && b_planes != 0) {
+          tma_load_3d_pair(dst, &map_b, kb * BK, b_row, 0, lead_full);
+        } else if (SWIGLU) {
+          tma_load_2d_pair(dst, &map_b, kb * BK, b_row, lead_full);
+          tma_load_2d_pair(dst + pair::B_BYTES / 2, &map_b_up, kb * BK, b_row, lead_full);
+        } else {
+          tma_load_2d_pair(dst, &map_b, kb * BK, b_row, lead_full);
+        }
         issued |= 1u << stage;
         issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
         if (++stage == S) { stage = 0; phase ^= 1u; }
@@ -562,6 +584,8 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
         int stage = 0, acc = 0;
         uint32_t phase = 0, acc_phase = 0;
         for (int tile = pair_id; tile < total_tiles; tile += npairs) {
+          const Tile tl = decode_rows<pair::PM>(tile, tile_start, G, offsets, M_total, NB);
+          const uint32_t idesc = tl.rows <= pair::PM / 2 ? pair::IDESC_HALF : pair::IDESC_FULL;
           if (!mbar_wait_cluster(tempty_bar(acc), acc_phase ^ 1u, abort_flag, status, true)) break;
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
@@ -573,7 +597,7 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
             const uint32_t b_base = a_base + pair::A_BYTES;
 #pragma unroll
             for (int k = 0; k < BK / UK; ++k)
-              tc_mma_pair(d_tmem, sw128_desc(a_base + k * UK * 2), sw128_desc(b_base + k * UK * 2), pair::IDESC,
+              tc_mma_pair(d_tmem, sw128_desc(a_base + k * UK * 2), sw128_desc(b_base + k * UK * 2), idesc,
                           (kb | k) != 0 ? 1u : 0u);
             tc_commit_pair(empty_bar(stage), 0x3);
             if (++stage == S) { stage = 0; phase ^= 1u; }
@@ -590,46 +614,59 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
   } else if (warp >= 2 && warp <= 5) {
     // ---------------- epilogue (warps 2..5 of both CTAs) ----------------
     const int q = warp & 3;  // TMEM lane quarter this warp may access
-    const int row_local = q * 32 + lane;
+    const int tlane = q * 32 + lane;
     const uint32_t lead_tempty0 = map_to_rank(tempty_bar(0), 0), lead_tempty1 = map_to_rank(tempty_bar(1), 0);
+    const int gate_first = b_planes != 2;  // plane order of each 64-row B block
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = pair_id; tile < total_tiles; tile += npairs) {
       const Tile tl = decode_rows<pair::PM>(tile, tile_start, G, offsets, M_total, NB);
+      const bool half = tl.rows <= pair::PM / 2;
       const bool ok = mbar_wait(tfull_bar(acc), acc_phase, abort_flag, status, true);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-      const int pr = (int)rank * BM + row_local;  // row within the pair tile
+      // half tile: lanes 0-63 hold the CTA's 64 rows for accumulator columns 0-127, lanes
+      // 64-127 the same rows for columns 128-255 (read back at TMEM columns 0-127)
+      const int row = half ? (tlane & 63) : tlane;
+      const int pr = (int)rank * (half ? BM / 2 : BM) + row;  // row within the pair tile
       const bool valid = pr < tl.rows;
       __nv_bfloat16* orow = out + (size_t)(tl.row0 + pr) * NOUT + tl.nb * TN;
       if (SWIGLU) {
+        // accumulator columns: [leader gate|up 64 + 64][other CTA gate|up 64 + 64]
+        const int fb0 = half ? (tlane >> 6) : 0, fb1 = half ? fb0 : 1;
+        for (int fb = fb0; fb <= fb1; ++fb) {
+          const uint32_t cb = half ? 0u : (uint32_t)(fb * 128);
+          const uint32_t gcol = cb + (gate_first ? 0u : 64u), ucol = cb + (gate_first ? 64u : 0u);
 #pragma unroll 1
-        for (int c = 0; c < TN / 32; ++c) {
-          uint32_t gv[32], uv[32];
-          tmem_ld32(taddr + c * 32, gv);
-          tmem_ld32(taddr + TN + c * 32, uv);
-          tmem_ld_wait();
-          if (valid && tl.nb * TN + c * 32 < NOUT) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+          for (int c = 0; c < 2; ++c) {
+            uint32_t gv[32], uv[32];
+            tmem_ld32(taddr + gcol + c * 32, gv);
+            tmem_ld32(taddr + ucol + c * 32, uv);
+            tmem_ld_wait();
+            const int f = fb * 64 + c * 32;  // output column within the tile
+            if (valid && tl.nb * TN + f < NOUT) {
+              uint4* dst = reinterpret_cast<uint4*>(orow + f);
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              float h[8];
+              for (int v = 0; v < 4; ++v) {
+                float h[8];
 #pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                const float g = __uint_as_float(gv[v * 8 + i]);
-                const float u = __uint_as_float(uv[v * 8 + i]);
-                h[i] = __fdividef(g, 1.0f + __expf(-g)) * u;
+                for (int i = 0; i < 8; ++i) {
+                  const float g = __uint_as_float(gv[v * 8 + i]);
+                  const float u = __uint_as_float(uv[v * 8 + i]);
+                  h[i] = __fdividef(g, 1.0f + __expf(-g)) * u;
+                }
+                dst[v] = f32_to_bf16x8(h);
               }
-              dst[v] = f32_to_bf16x8(h);
             }
           }
         }
       } else {
+        const int c0 = half ? (tlane >> 6) * 4 : 0, c1 = half ? c0 + 4 : 8;  // 32-column chunks
 #pragma unroll 1
-        for (int c = 0; c < TN / 32; ++c) {
+        for (int c = c0; c < c1; ++c) {
           uint32_t yv[32];
-          tmem_ld32(taddr + c * 32, yv);
+          tmem_ld32(taddr + (uint32_t)((c - (half ? c0 : 0)) * 32), yv);
           tmem_ld_wait();
           if (valid && tl.nb * TN + c * 32 < NOUT) {
             uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
@@ -738,8 +775,9 @@ moe_status_t launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorM
 size_t pair_smem_bytes(int G) { return 1024 + (size_t)pair::STAGES * pair::STAGE_BYTES + 256 + (size_t)(G + 16) * 4; }
 
 template <int MODE>
-moe_status_t launch_pair(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1, const int32_t* offsets,
-                         int G, int M_total, int K, int NOUT, void* out, int* status, cudaStream_t s) {
+moe_status_t launch_pair(const CUtensorMap& a, const CUtensorMap& a_half, const CUtensorMap& b,
+                         const CUtensorMap& b_up, int b_planes, const int32_t* offsets, int G, int M_total, int K,
+                         int NOUT, void* out, int* status, cudaStream_t s) {
   const size_t smem = pair_smem_bytes(G);
   auto kern = pair_gemm_kernel<MODE>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
@@ -748,7 +786,7 @@ moe_status_t launch_pair(const CUtensorMap& a, const CUtensorMap& b0, const CUte
   const long long NB = (NOUT + TN - 1) / TN;
   const long long max_tiles = ((long long)(M_total + pair::PM - 1) / pair::PM + G) * NB;
   const int pairs = (int)std::min<long long>(max_tiles, (long long)(sm_count() / 2));
-  kern<<<2 * pairs, pair::THREADS, smem, s>>>(a, b0, b1, offsets, G, M_total, K, NOUT,
+  kern<<<2 * pairs, pair::THREADS, smem, s>>>(a, a_half, b, b_up, offsets, G, M_total, K, NOUT, b_planes,
                                               static_cast<__nv_bfloat16*>(out), status);
   return launch_status();
 }
@@ -852,16 +890,25 @@ extern "C" moe_status_t moe_grouped_swiglu(const void* x_perm, moe_dtype_t dtype
   int* status = device_status_word();
   if (!status) return MOE_ERR_CUDA;
   if (tc::use_pair(G, M_total)) {
-    CUtensorMap ma, mg, mu, mh, md;
+    CUtensorMap ma, ma2, mg, mu, mh, mh2, md, mgu;
     if (!tc::make_map_bf16(&ma, x_perm, (uint64_t)M_total, (uint64_t)D, tc::BM) ||
-        !tc::make_map_bf16(&mg, w_gate, (uint64_t)G * F, (uint64_t)D, tc::pair::HB) ||
-        !tc::make_map_bf16(&mu, w_up, (uint64_t)G * F, (uint64_t)D, tc::pair::HB) ||
+        !tc::make_map_bf16(&ma2, x_perm, (uint64_t)M_total, (uint64_t)D, tc::BM / 2) ||
         !tc::make_map_bf16(&mh, h_workspace, (uint64_t)M_total, (uint64_t)F, tc::BM) ||
+        !tc::make_map_bf16(&mh2, h_workspace, (uint64_t)M_total, (uint64_t)F, tc::BM / 2) ||
         !tc::make_map_bf16(&md, w_down, (uint64_t)G * D, (uint64_t)F, tc::pair::HB))
       return MOE_ERR_CUDA;
-    moe_status_t st = tc::launch_pair<0>(ma, mg, mu, offsets, G, M_total, D, F, h_workspace, status, s);
+    int planes = 0;
+    moe_status_t st;
+    if (tc::make_map_gate_up(&mgu, w_gate, w_up, (uint64_t)G * F, (uint64_t)D, tc::BN / 4, &planes)) {
+      st = tc::launch_pair<0>(ma, ma2, mgu, mgu, planes, offsets, G, M_total, D, F, h_workspace, status, s);
+    } else {
+      if (!tc::make_map_bf16(&mg, w_gate, (uint64_t)G * F, (uint64_t)D, tc::BN / 4) ||
+          !tc::make_map_bf16(&mu, w_up, (uint64_t)G * F, (uint64_t)D, tc::BN / 4))
+        return MOE_ERR_CUDA;
+      st = tc::launch_pair<0>(ma, ma2, mg, mu, 0, offsets, G, M_total, D, F, h_workspace, status, s);
+    }
     if (st != MOE_OK) return st;
-    return tc::launch_pair<1>(mh, md, md, offsets, G, M_total, F, D, y_perm, status, s);
+    return tc::launch_pair<1>(mh, mh2, md, md, 0, offsets, G, M_total, F, D, y_perm, status, s);
   }
   CUtensorMap ma, mg, mu, mh, md;
   if (!tc::make_map_bf16(&ma, x_perm, (uint64_t)M_total, (uint64_t)D, tc::BM) ||
