@@ -16,8 +16,8 @@
 //     (measured 8e-8 rms, about the fp32 rounding of the result);
 //   * the mid and lo planes, stacked as one N = 2*NT operand, accumulate across the whole
 //     reduction in a second accumulator: their error is scaled down by 2^-8.
-// An M=128 MMA costs about the same time for any N up to 256 (measured), so this takes 8
-// MMAs per slice instead of 12.  The hand-off per slice is one mbarrier arrival per
+// Stacking mid and lo makes 8 MMAs per slice instead of 12 (an M=128 MMA costs 48, 64 and
+// 128 SM cycles at N = 64, 128 and 256, measured).  The hand-off per slice is one mbarrier arrival per
 // epilogue warp and a plain add per column, folded into the compensated total every 8
 // slices.  Short token counts are split along D (split-K) so that about
 // 128 CTAs stream the activations; the top-k kernel adds the split partials in order.
