@@ -435,6 +435,7 @@ constexpr int A_BYTES = BM * BK * 2;     // 16 KB (8 KB used by a half tile)
 constexpr int B_BYTES = HB * BK * 2;     // 16 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int THREADS = 224;             // warps: 0 B copies, 1 MMA, 2-5 epilogue, 6 A copies
+constexpr int STAGING_BYTES = 32 * 128;  // one 32-row x 64-column bf16 output block
 constexpr uint32_t IDESC_FULL = idesc_bf16(PM, BN);
 constexpr uint32_t IDESC_HALF = idesc_bf16(PM / 2, BN);
 }  // namespace pair
@@ -447,14 +448,17 @@ template <int MODE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::THREADS, 1)
 pair_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_a_half,
                  const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUtensorMap map_b_up,
-                 const int32_t* __restrict__ offsets, int G, int M_total, int K, int NOUT, int b_planes,
-                 __nv_bfloat16* __restrict__ out, int* __restrict__ status) {
+                 const __grid_constant__ CUtensorMap map_out, const int32_t* __restrict__ offsets, int G,
+                 int M_total, int K, int NOUT, int b_planes, int nbuf, __nv_bfloat16* __restrict__ out,
+                 int* __restrict__ status) {
   constexpr bool SWIGLU = MODE == 0;
   constexpr int TN = SWIGLU ? BN / 2 : BN;  // output columns per tile
   constexpr int S = pair::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * pair::STAGE_BYTES);
+  // output staging: nbuf 4 KB buffers (32 rows x 64 bf16, 128-byte swizzle) per epilogue warp
+  uint8_t* staging = smem + S * pair::STAGE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(staging + 4 * nbuf * pair::STAGING_BYTES);
   // bars: full[S] (leader's are used), empty[S], tfull[2], tempty[2] (leader's), done
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
@@ -613,11 +617,16 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
     }
   } else if (warp >= 2 && warp <= 5) {
     // ---------------- epilogue (warps 2..5 of both CTAs) ----------------
+    // Each warp owns 32 rows of the tile and writes them in 64-column blocks: the block is
+    // packed to bf16, staged in shared memory in the 128-byte swizzled layout and stored by
+    // one TMA bulk store; a block that crosses the end of its expert's rows (the next
+    // expert's rows follow in memory) is written row by row from registers instead.
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int tlane = q * 32 + lane;
     const uint32_t lead_tempty0 = map_to_rank(tempty_bar(0), 0), lead_tempty1 = map_to_rank(tempty_bar(1), 0);
     const int gate_first = b_planes != 2;  // plane order of each 64-row B block
-    int acc = 0;
+    const uint32_t my_staging = smem_u32(staging) + (uint32_t)(q * nbuf * pair::STAGING_BYTES);
+    int acc = 0, bi = 0, stores = 0;
     uint32_t acc_phase = 0;
     for (int tile = pair_id; tile < total_tiles; tile += npairs) {
       const Tile tl = decode_rows<pair::PM>(tile, tile_start, G, offsets, M_total, NB);
@@ -629,55 +638,81 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
       // half tile: lanes 0-63 hold the CTA's 64 rows for accumulator columns 0-127, lanes
       // 64-127 the same rows for columns 128-255 (read back at TMEM columns 0-127)
       const int row = half ? (tlane & 63) : tlane;
-      const int pr = (int)rank * (half ? BM / 2 : BM) + row;  // row within the pair tile
+      const int pr_base = (int)rank * (half ? BM / 2 : BM) + (row & ~31);  // first row of the warp
+      const int pr = pr_base + lane;                                          // row within the tile
       const bool valid = pr < tl.rows;
-      __nv_bfloat16* orow = out + (size_t)(tl.row0 + pr) * NOUT + tl.nb * TN;
-      if (SWIGLU) {
-        // accumulator columns: [leader gate|up 64 + 64][other CTA gate|up 64 + 64]
-        const int fb0 = half ? (tlane >> 6) : 0, fb1 = half ? fb0 : 1;
-        for (int fb = fb0; fb <= fb1; ++fb) {
+      const bool whole = pr_base + 32 <= tl.rows;  // warp-uniform
+      const int units = SWIGLU ? (half ? 1 : 2) : (half ? 2 : 4);
+#pragma unroll 1
+      for (int u = 0; u < units; ++u) {
+        // accumulator columns of this 64-column block and its output columns in the tile
+        int ocol;
+        uint32_t c_a, c_b;  // SwiGLU: gate and up TMEM columns; down: TMEM column
+        if (SWIGLU) {
+          const int fb = half ? (tlane >> 6) : u;  // [leader gate|up 64+64][other CTA gate|up]
           const uint32_t cb = half ? 0u : (uint32_t)(fb * 128);
-          const uint32_t gcol = cb + (gate_first ? 0u : 64u), ucol = cb + (gate_first ? 64u : 0u);
-#pragma unroll 1
-          for (int c = 0; c < 2; ++c) {
-            uint32_t gv[32], uv[32];
-            tmem_ld32(taddr + gcol + c * 32, gv);
-            tmem_ld32(taddr + ucol + c * 32, uv);
-            tmem_ld_wait();
-            const int f = fb * 64 + c * 32;  // output column within the tile
-            if (valid && tl.nb * TN + f < NOUT) {
-              uint4* dst = reinterpret_cast<uint4*>(orow + f);
-#pragma unroll
-              for (int v = 0; v < 4; ++v) {
-                float h[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                  const float g = __uint_as_float(gv[v * 8 + i]);
-                  const float u = __uint_as_float(uv[v * 8 + i]);
-                  h[i] = __fdividef(g, 1.0f + __expf(-g)) * u;
-                }
-                dst[v] = f32_to_bf16x8(h);
-              }
-            }
-          }
+          c_a = cb + (gate_first ? 0u : 64u);
+          c_b = cb + (gate_first ? 64u : 0u);
+          ocol = fb * 64;
+        } else {
+          c_a = (uint32_t)(u * 64);
+          c_b = 0;
+          ocol = (half ? (tlane >> 6) * 128 : 0) + u * 64;
         }
-      } else {
-        const int c0 = half ? (tlane >> 6) * 4 : 0, c1 = half ? c0 + 4 : 8;  // 32-column chunks
-#pragma unroll 1
-        for (int c = c0; c < c1; ++c) {
-          uint32_t yv[32];
-          tmem_ld32(taddr + (uint32_t)((c - (half ? c0 : 0)) * 32), yv);
-          tmem_ld_wait();
-          if (valid && tl.nb * TN + c * 32 < NOUT) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+        if (tl.nb * TN + ocol >= NOUT) continue;  // column tail (warp-uniform)
+        uint4 packed[8];
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          if (SWIGLU) {
+            uint32_t gv[32], uv[32];
+            tmem_ld32(taddr + c_a + c * 32, gv);
+            tmem_ld32(taddr + c_b + c * 32, uv);
+            tmem_ld_wait();
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              float h[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const float g = __uint_as_float(gv[v * 8 + i]);
+                const float uu = __uint_as_float(uv[v * 8 + i]);
+                h[i] = __fdividef(g, 1.0f + __expf(-g)) * uu;
+              }
+              packed[c * 4 + v] = f32_to_bf16x8(h);
+            }
+          } else {
+            uint32_t yv[32];
+            tmem_ld32(taddr + c_a + c * 32, yv);
+            tmem_ld_wait();
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
               float y[8];
 #pragma unroll
               for (int i = 0; i < 8; ++i) y[i] = __uint_as_float(yv[v * 8 + i]);
-              dst[v] = f32_to_bf16x8(y);
+              packed[c * 4 + v] = f32_to_bf16x8(y);
             }
           }
+        }
+        if (whole) {
+          const uint32_t buf = my_staging + (uint32_t)(bi * pair::STAGING_BYTES);
+          if (lane == 0 && stores >= nbuf) {  // this buffer's previous store has read it
+            if (nbuf == 2) bulk_wait_read<1>(); else bulk_wait_read<0>();
+          }
+          __syncwarp();
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            st_shared_v4(buf + (uint32_t)(lane * 128) + ((uint32_t)(c ^ (lane & 7)) << 4), packed[c]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&map_out, tl.nb * TN + ocol, tl.row0 + pr_base, buf);
+            bulk_commit();
+          }
+          ++stores;
+          if (++bi == nbuf) bi = 0;
+        } else if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(out + (size_t)(tl.row0 + pr) * NOUT + tl.nb * TN + ocol);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) dst[c] = packed[c];
         }
       }
       tc_fence_before();
@@ -688,6 +723,7 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
       }
       if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
     }
+    if (lane == 0) bulk_wait_all();  // every store has left shared memory and landed
   }
 
   tc_fence_before();
@@ -772,13 +808,17 @@ moe_status_t launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorM
   return launch_status();
 }
 
-size_t pair_smem_bytes(int G) { return 1024 + (size_t)pair::STAGES * pair::STAGE_BYTES + 256 + (size_t)(G + 16) * 4; }
+size_t pair_smem_bytes(int G, int nbuf) {
+  return 1024 + (size_t)pair::STAGES * pair::STAGE_BYTES + (size_t)4 * nbuf * pair::STAGING_BYTES + 256 +
+         (size_t)(G + 16) * 4;
+}
 
 template <int MODE>
 moe_status_t launch_pair(const CUtensorMap& a, const CUtensorMap& a_half, const CUtensorMap& b,
-                         const CUtensorMap& b_up, int b_planes, const int32_t* offsets, int G, int M_total, int K,
-                         int NOUT, void* out, int* status, cudaStream_t s) {
-  const size_t smem = pair_smem_bytes(G);
+                         const CUtensorMap& b_up, const CUtensorMap& out_map, int b_planes, const int32_t* offsets,
+                         int G, int M_total, int K, int NOUT, void* out, int* status, cudaStream_t s) {
+  const int nbuf = pair_smem_bytes(G, 2) <= 227 * 1024 ? 2 : 1;  // double-buffer the staging if it fits
+  const size_t smem = pair_smem_bytes(G, nbuf);
   auto kern = pair_gemm_kernel<MODE>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return MOE_ERR_CUDA;
@@ -786,8 +826,8 @@ moe_status_t launch_pair(const CUtensorMap& a, const CUtensorMap& a_half, const 
   const long long NB = (NOUT + TN - 1) / TN;
   const long long max_tiles = ((long long)(M_total + pair::PM - 1) / pair::PM + G) * NB;
   const int pairs = (int)std::min<long long>(max_tiles, (long long)(sm_count() / 2));
-  kern<<<2 * pairs, pair::THREADS, smem, s>>>(a, a_half, b, b_up, offsets, G, M_total, K, NOUT, b_planes,
-                                              static_cast<__nv_bfloat16*>(out), status);
+  kern<<<2 * pairs, pair::THREADS, smem, s>>>(a, a_half, b, b_up, out_map, offsets, G, M_total, K, NOUT, b_planes,
+                                              nbuf, static_cast<__nv_bfloat16*>(out), status);
   return launch_status();
 }
 
@@ -890,8 +930,10 @@ extern "C" moe_status_t moe_grouped_swiglu(const void* x_perm, moe_dtype_t dtype
   int* status = device_status_word();
   if (!status) return MOE_ERR_CUDA;
   if (tc::use_pair(G, M_total)) {
-    CUtensorMap ma, ma2, mg, mu, mh, mh2, md, mgu;
-    if (!tc::make_map_bf16(&ma, x_perm, (uint64_t)M_total, (uint64_t)D, tc::BM) ||
+    CUtensorMap ma, ma2, mg, mu, mh, mh2, md, mgu, mho, myo;
+    if (!tc::make_map_bf16(&mho, h_workspace, (uint64_t)M_total, (uint64_t)F, 32) ||
+        !tc::make_map_bf16(&myo, y_perm, (uint64_t)M_total, (uint64_t)D, 32) ||
+        !tc::make_map_bf16(&ma, x_perm, (uint64_t)M_total, (uint64_t)D, tc::BM) ||
         !tc::make_map_bf16(&ma2, x_perm, (uint64_t)M_total, (uint64_t)D, tc::BM / 2) ||
         !tc::make_map_bf16(&mh, h_workspace, (uint64_t)M_total, (uint64_t)F, tc::BM) ||
         !tc::make_map_bf16(&mh2, h_workspace, (uint64_t)M_total, (uint64_t)F, tc::BM / 2) ||
@@ -900,15 +942,15 @@ extern "C" moe_status_t moe_grouped_swiglu(const void* x_perm, moe_dtype_t dtype
     int planes = 0;
     moe_status_t st;
     if (tc::make_map_gate_up(&mgu, w_gate, w_up, (uint64_t)G * F, (uint64_t)D, tc::BN / 4, &planes)) {
-      st = tc::launch_pair<0>(ma, ma2, mgu, mgu, planes, offsets, G, M_total, D, F, h_workspace, status, s);
+      st = tc::launch_pair<0>(ma, ma2, mgu, mgu, mho, planes, offsets, G, M_total, D, F, h_workspace, status, s);
     } else {
       if (!tc::make_map_bf16(&mg, w_gate, (uint64_t)G * F, (uint64_t)D, tc::BN / 4) ||
           !tc::make_map_bf16(&mu, w_up, (uint64_t)G * F, (uint64_t)D, tc::BN / 4))
         return MOE_ERR_CUDA;
-      st = tc::launch_pair<0>(ma, ma2, mg, mu, 0, offsets, G, M_total, D, F, h_workspace, status, s);
+      st = tc::launch_pair<0>(ma, ma2, mg, mu, mho, 0, offsets, G, M_total, D, F, h_workspace, status, s);
     }
     if (st != MOE_OK) return st;
-    return tc::launch_pair<1>(mh, mh2, md, md, 0, offsets, G, M_total, F, D, y_perm, status, s);
+    return tc::launch_pair<1>(mh, mh2, md, md, myo, 0, offsets, G, M_total, F, D, y_perm, status, s);
   }
   CUtensorMap ma, mg, mu, mh, md;
   if (!tc::make_map_bf16(&ma, x_perm, (uint64_t)M_total, (uint64_t)D, tc::BM) ||
