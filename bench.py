@@ -158,7 +158,7 @@ class Step:
 
     STAGES = ("router", "permute", "grouped_swiglu", "shared", "combine", "bias")
 
-    def __init__(self, cfg, dev, rank, world, gather=False):
+    def __init__(self, cfg, dev, rank, world, gather=None):
         self.cfg, self.dev, self.world = cfg, dev, world
         seed_tok = cfg.seed + 1000 * rank
         xn, h = synth.make_tokens(cfg, dev, seed=seed_tok)
@@ -345,9 +345,12 @@ def main():
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--gather", action="store_true",
-                    help="GEMM1 gathers its rows from xn through perm_token (no x_perm); "
-                         "default: the permute writes x_perm and GEMM1 loads it by TMA")
+    rows = ap.add_mutually_exclusive_group()
+    rows.add_argument("--permute-copy", action="store_true",
+                      help="the permute writes the permuted rows x_perm and GEMM1 loads them by TMA")
+    rows.add_argument("--gather", action="store_true",
+                      help="GEMM1 gathers its rows from xn through perm_token (default: the layer "
+                           "chooses by size)")
     args = ap.parse_args()
     cfg = synth.CONFIGS[args.config]
     if args.impl == "reference":
@@ -364,7 +367,7 @@ def main():
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
     dev = torch.device("cuda", local)
 
-    step = Step(cfg, dev, rank, world, gather=args.gather)
+    step = Step(cfg, dev, rank, world, gather=True if args.gather else (False if args.permute_copy else None))
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         total_ms, stage_us = time_device(step, args.steps, args.warmup, world)

@@ -45,6 +45,7 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int THREADS = 192;
 constexpr int TMEM_COLS = 512;
 constexpr int MAX_GROUPS = 1024;
+constexpr int STAGING_BYTES = 32 * 128;  // one 32-row x 64-column bf16 output block
 
 constexpr uint32_t IDESC = idesc_bf16(BM, BN);
 
@@ -101,16 +102,18 @@ static_assert(GATHER_LAG >= 0 && GATHER_LAG < STAGES, "gather lag must leave a s
 template <int MODE>
 __global__ void __launch_bounds__(kThreads<MODE>, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b0,
-                    const __grid_constant__ CUtensorMap map_b1, const int32_t* __restrict__ offsets,
-                    int G, int M_total, int K, int NOUT, __nv_bfloat16* __restrict__ out,
-                    const __nv_bfloat16* __restrict__ xg, int NX, const int32_t* __restrict__ perm,
-                    int b_planes, int* __restrict__ status) {
+                    const __grid_constant__ CUtensorMap map_b1, const __grid_constant__ CUtensorMap map_out,
+                    const int32_t* __restrict__ offsets, int G, int M_total, int K, int NOUT,
+                    __nv_bfloat16* __restrict__ out, const __nv_bfloat16* __restrict__ xg, int NX,
+                    const int32_t* __restrict__ perm, int b_planes, int nbuf, int* __restrict__ status) {
   constexpr bool SWIGLU = MODE != 1;
   constexpr int TN = SWIGLU ? BN / 2 : BN;  // output columns per tile
   constexpr int NTHR = kThreads<MODE>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  // output staging: nbuf 4 KB buffers (32 rows x 64 bf16, 128-byte swizzle) per epilogue warp
+  uint8_t* staging = smem + STAGES * STAGE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(staging + 4 * nbuf * STAGING_BYTES);
   // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], done
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
@@ -344,9 +347,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
     }
   } else {
     // ---------------- epilogue (warps 2..5) ----------------
+    // Each warp owns 32 rows of the tile and writes them in 64-column blocks through a
+    // swizzled shared-memory buffer and one TMA bulk store (row by row from registers when
+    // the block crosses the end of its group's rows), as in the CTA-pair kernel.
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row_local = q * 32 + lane;
-    int acc = 0;
+    const uint32_t my_staging = smem_u32(staging) + (uint32_t)(q * nbuf * STAGING_BYTES);
+    const uint32_t gcol = b_planes == 2 ? TN : 0;  // up rows came first in B
+    int acc = 0, bi = 0, stores = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
       const Tile tl = decode(tile, tile_start, G, offsets, M_total, NB);
@@ -355,46 +363,64 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
       const bool valid = row_local < tl.rows;
-      __nv_bfloat16* orow = out + (size_t)(tl.row0 + row_local) * NOUT + tl.nb * TN;
-      if (SWIGLU) {
+      const bool whole = q * 32 + 32 <= tl.rows;  // warp-uniform
 #pragma unroll 1
-        for (int c = 0; c < TN / 32; ++c) {
-          uint32_t gv[32], uv[32];
-          const uint32_t gcol = b_planes == 2 ? TN : 0;  // up rows came first in B
-          tmem_ld32(taddr + gcol + c * 32, gv);
-          tmem_ld32(taddr + (TN - gcol) + c * 32, uv);
-          tmem_ld_wait();
-          if (valid && tl.nb * TN + c * 32 < NOUT) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+      for (int u = 0; u < TN / 64; ++u) {
+        const int ocol = u * 64;
+        if (tl.nb * TN + ocol >= NOUT) continue;  // column tail (warp-uniform)
+        uint4 packed[8];
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          if (SWIGLU) {
+            uint32_t gv[32], uv[32];
+            tmem_ld32(taddr + gcol + ocol + c * 32, gv);
+            tmem_ld32(taddr + (TN - gcol) + ocol + c * 32, uv);
+            tmem_ld_wait();
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
               float h[8];
 #pragma unroll
               for (int i = 0; i < 8; ++i) {
                 const float g = __uint_as_float(gv[v * 8 + i]);
-                const float u = __uint_as_float(uv[v * 8 + i]);
-                h[i] = __fdividef(g, 1.0f + __expf(-g)) * u;
+                const float uu = __uint_as_float(uv[v * 8 + i]);
+                h[i] = __fdividef(g, 1.0f + __expf(-g)) * uu;
               }
-              dst[v] = f32_to_bf16x8(h);
+              packed[c * 4 + v] = f32_to_bf16x8(h);
             }
-          }
-        }
-      } else {
-#pragma unroll 1
-        for (int c = 0; c < TN / 32; ++c) {
-          uint32_t yv[32];
-          tmem_ld32(taddr + c * 32, yv);
-          tmem_ld_wait();
-          if (valid && tl.nb * TN + c * 32 < NOUT) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+          } else {
+            uint32_t yv[32];
+            tmem_ld32(taddr + ocol + c * 32, yv);
+            tmem_ld_wait();
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
               float y[8];
 #pragma unroll
               for (int i = 0; i < 8; ++i) y[i] = __uint_as_float(yv[v * 8 + i]);
-              dst[v] = f32_to_bf16x8(y);
+              packed[c * 4 + v] = f32_to_bf16x8(y);
             }
           }
+        }
+        if (whole) {
+          const uint32_t buf = my_staging + (uint32_t)(bi * STAGING_BYTES);
+          if (lane == 0 && stores >= nbuf) {  // this buffer's previous store has read it
+            if (nbuf == 2) bulk_wait_read<1>(); else bulk_wait_read<0>();
+          }
+          __syncwarp();
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            st_shared_v4(buf + (uint32_t)(lane * 128) + ((uint32_t)(c ^ (lane & 7)) << 4), packed[c]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&map_out, tl.nb * TN + ocol, tl.row0 + q * 32, buf);
+            bulk_commit();
+          }
+          ++stores;
+          if (++bi == nbuf) bi = 0;
+        } else if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(out + (size_t)(tl.row0 + row_local) * NOUT + tl.nb * TN + ocol);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) dst[c] = packed[c];
         }
       }
       tc_fence_before();
@@ -402,6 +428,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
       if (lane == 0) mbar_arrive(tempty_bar(acc));
       if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
     }
+    if (lane == 0) bulk_wait_all();  // every store has left shared memory and landed
   }
 
   tc_fence_before();
@@ -788,13 +815,17 @@ bool make_map_gate_up(CUtensorMap* m, const void* w_gate, const void* w_up, uint
   return true;
 }
 
-size_t smem_bytes(int G) { return 1024 + (size_t)STAGES * STAGE_BYTES + 256 + (size_t)(G + 32) * 4; }
+size_t smem_bytes(int G, int nbuf) {
+  return 1024 + (size_t)STAGES * STAGE_BYTES + (size_t)4 * nbuf * STAGING_BYTES + 256 + (size_t)(G + 32) * 4;
+}
 
 template <int MODE>
-moe_status_t launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1, const int32_t* offsets,
-                    int G, int M_total, int K, int NOUT, void* out, int* status, cudaStream_t s,
-                    const void* xg = nullptr, int NX = 0, const int32_t* perm = nullptr, int b_planes = 0) {
-  const size_t smem = smem_bytes(G);
+moe_status_t launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1, const CUtensorMap& out_map,
+                    const int32_t* offsets, int G, int M_total, int K, int NOUT, void* out, int* status,
+                    cudaStream_t s, const void* xg = nullptr, int NX = 0, const int32_t* perm = nullptr,
+                    int b_planes = 0) {
+  const int nbuf = smem_bytes(G, 2) <= 227 * 1024 ? 2 : 1;  // double-buffer the staging if it fits
+  const size_t smem = smem_bytes(G, nbuf);
   auto kern = grouped_gemm_kernel<MODE>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return MOE_ERR_CUDA;
@@ -802,9 +833,9 @@ moe_status_t launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorM
   const long long NB = (NOUT + TN - 1) / TN;
   const long long max_tiles = ((long long)(M_total + BM - 1) / BM + G) * NB;
   const int grid = (int)std::min<long long>(max_tiles, (long long)sm_count());
-  kern<<<grid, kThreads<MODE>, smem, s>>>(a, b0, b1, offsets, G, M_total, K, NOUT,
+  kern<<<grid, kThreads<MODE>, smem, s>>>(a, b0, b1, out_map, offsets, G, M_total, K, NOUT,
                                           static_cast<__nv_bfloat16*>(out),
-                                          static_cast<const __nv_bfloat16*>(xg), NX, perm, b_planes, status);
+                                          static_cast<const __nv_bfloat16*>(xg), NX, perm, b_planes, nbuf, status);
   return launch_status();
 }
 
@@ -952,21 +983,23 @@ extern "C" moe_status_t moe_grouped_swiglu(const void* x_perm, moe_dtype_t dtype
     if (st != MOE_OK) return st;
     return tc::launch_pair<1>(mh, mh2, md, md, myo, 0, offsets, G, M_total, F, D, y_perm, status, s);
   }
-  CUtensorMap ma, mg, mu, mh, md;
+  CUtensorMap ma, mg, mu, mh, md, mho, myo;
   if (!tc::make_map_bf16(&ma, x_perm, (uint64_t)M_total, (uint64_t)D, tc::BM) ||
       !tc::make_map_bf16(&mg, w_gate, (uint64_t)G * F, (uint64_t)D, tc::BN / 2) ||
       !tc::make_map_bf16(&mu, w_up, (uint64_t)G * F, (uint64_t)D, tc::BN / 2) ||
       !tc::make_map_bf16(&mh, h_workspace, (uint64_t)M_total, (uint64_t)F, tc::BM) ||
-      !tc::make_map_bf16(&md, w_down, (uint64_t)G * D, (uint64_t)F, tc::BN))
+      !tc::make_map_bf16(&md, w_down, (uint64_t)G * D, (uint64_t)F, tc::BN) ||
+      !tc::make_map_bf16(&mho, h_workspace, (uint64_t)M_total, (uint64_t)F, 32) ||
+      !tc::make_map_bf16(&myo, y_perm, (uint64_t)M_total, (uint64_t)D, 32))
     return MOE_ERR_CUDA;
   CUtensorMap mgu;
   int planes = 0;
   const bool gu = tc::make_map_gate_up(&mgu, w_gate, w_up, (uint64_t)G * F, (uint64_t)D, tc::BN / 2, &planes);
-  moe_status_t st = gu ? tc::launch<0>(ma, mgu, mgu, offsets, G, M_total, D, F, h_workspace, status, s, nullptr, 0,
-                                       nullptr, planes)
-                       : tc::launch<0>(ma, mg, mu, offsets, G, M_total, D, F, h_workspace, status, s);
+  moe_status_t st = gu ? tc::launch<0>(ma, mgu, mgu, mho, offsets, G, M_total, D, F, h_workspace, status, s,
+                                       nullptr, 0, nullptr, planes)
+                       : tc::launch<0>(ma, mg, mu, mho, offsets, G, M_total, D, F, h_workspace, status, s);
   if (st != MOE_OK) return st;
-  return tc::launch<1>(mh, md, md, offsets, G, M_total, F, D, y_perm, status, s);
+  return tc::launch<1>(mh, md, md, myo, offsets, G, M_total, F, D, y_perm, status, s);
 }
 
 extern "C" moe_status_t moe_grouped_swiglu_gather(const void* xn, int N, const int32_t* perm_token,
@@ -987,19 +1020,21 @@ extern "C" moe_status_t moe_grouped_swiglu_gather(const void* xn, int N, const i
   int* status = device_status_word();
   if (!status) return MOE_ERR_CUDA;
   cudaStream_t s = as_cuda(stream);
-  CUtensorMap mg, mu, mh, md;
+  CUtensorMap mg, mu, mh, md, mho, myo;
   if (!tc::make_map_bf16(&mg, w_gate, (uint64_t)G * F, (uint64_t)D, tc::BN / 2) ||
       !tc::make_map_bf16(&mu, w_up, (uint64_t)G * F, (uint64_t)D, tc::BN / 2) ||
       !tc::make_map_bf16(&mh, h_workspace, (uint64_t)M_total, (uint64_t)F, tc::BM) ||
-      !tc::make_map_bf16(&md, w_down, (uint64_t)G * D, (uint64_t)F, tc::BN))
+      !tc::make_map_bf16(&md, w_down, (uint64_t)G * D, (uint64_t)F, tc::BN) ||
+      !tc::make_map_bf16(&mho, h_workspace, (uint64_t)M_total, (uint64_t)F, 32) ||
+      !tc::make_map_bf16(&myo, y_perm, (uint64_t)M_total, (uint64_t)D, 32))
     return MOE_ERR_CUDA;
   CUtensorMap mgu;
   int planes = 0;
   const bool gu = tc::make_map_gate_up(&mgu, w_gate, w_up, (uint64_t)G * F, (uint64_t)D, tc::BN / 2, &planes);
-  moe_status_t st = gu ? tc::launch<2>(mgu, mgu, mgu, offsets, G, M_total, D, F, h_workspace, status, s, xn, N,
-                                       perm_token, planes)
-                       : tc::launch<2>(mg, mg, mu, offsets, G, M_total, D, F, h_workspace, status, s, xn, N,
+  moe_status_t st = gu ? tc::launch<2>(mgu, mgu, mgu, mho, offsets, G, M_total, D, F, h_workspace, status, s, xn,
+                                       N, perm_token, planes)
+                       : tc::launch<2>(mg, mg, mu, mho, offsets, G, M_total, D, F, h_workspace, status, s, xn, N,
                                        perm_token);
   if (st != MOE_OK) return st;
-  return tc::launch<1>(mh, md, md, offsets, G, M_total, F, D, y_perm, status, s);
+  return tc::launch<1>(mh, md, md, myo, offsets, G, M_total, F, D, y_perm, status, s);
 }

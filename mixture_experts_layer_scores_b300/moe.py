@@ -328,10 +328,13 @@ class MoELayer:
     """Top-k MoE FFN layer forward on one GPU, with reusable device buffers."""
 
     def __init__(self, weights: LayerWeights, N: int, k: int, score_fn="softmax", gamma=1e-3,
-                 dtype=torch.bfloat16, capacity_factor=None, gather=False):
-        """gather: (bf16) the first expert GEMM reads its rows from xn through perm_token
-        instead of from a permuted copy, which is then never written.  Off by default: the
-        gathered GEMM costs about as much time as the row copy it removes."""
+                 dtype=torch.bfloat16, capacity_factor=None, gather=None):
+        """gather (bf16): the first expert GEMM reads its rows from xn through perm_token
+        instead of from a permuted copy, which is then never written; False writes x_perm in
+        the permute and runs the GEMM on it.  None chooses by size: gathering costs the GEMM
+        roughly a tenth of its first half, the copy moves (1 + k) N D bf16 values, so it
+        gathers when d_ff * k / (k + 1) <= 1024 (measured: faster on the handbook and skewed
+        layers, slower on the Mixtral- and DeepSeek-V3-shaped ones)."""
         w = weights
         self.w, self.k, self.score_fn, self.gamma = w, k, score_fn, gamma
         E = w.w_router.shape[0]
@@ -350,7 +353,9 @@ class MoELayer:
         self.offsets = e(self.E + 1)
         self.row_map = e(N, k)
         self.perm_token = e(R)
-        self.gather = gather and dtype == torch.bfloat16
+        if gather is None:
+            gather = w.w_gate.shape[1] * k / (k + 1) <= 1024
+        self.gather = bool(gather) and dtype == torch.bfloat16
         self.x_perm = None if self.gather else e(R, self.D, dt=dtype)
         self.h_ws = e(R, self.F, dt=dtype)
         self.y_perm = e(R, self.D, dt=dtype)

@@ -75,15 +75,20 @@ def test_full_size_layer(name, k):
                                         "offsets": layer.offsets.cpu(), "row_map": layer.row_map.cpu(),
                                         "perm_token": layer.perm_token.cpu()}, cfg.E, k)
     perm_t = layer.perm_token.long()
-    assert torch.equal(layer.x_perm, xn[perm_t])                      # permuted rows exact
-    # the same GEMM reading its rows from xn through perm_token: the same bits
+    # the GEMM over the permuted copy and the GEMM gathering its rows from xn through
+    # perm_token (whichever the layer ran): the same bits
     w = layer.w
-    y_gather = moe.moe_grouped_swiglu_gather(xn, layer.perm_token, layer.offsets, w.w_gate, w.w_up,
-                                             w.w_down)
+    x_perm = layer.x_perm if layer.x_perm is not None else xn[perm_t]
+    assert torch.equal(x_perm, xn[perm_t])                            # permuted rows exact
+    if layer.x_perm is None:
+        y_other = moe.moe_grouped_swiglu(x_perm, layer.offsets, w.w_gate, w.w_up, w.w_down)
+    else:
+        y_other = moe.moe_grouped_swiglu_gather(xn, layer.perm_token, layer.offsets, w.w_gate, w.w_up,
+                                                w.w_down)
     torch.cuda.synchronize()
     assert moe.last_device_status() == 0
-    assert torch.equal(y_gather, layer.y_perm)
-    del y_gather
+    assert torch.equal(y_other, layer.y_perm)
+    del y_other, x_perm
 
     # --- the combine, every token (property) -------------------------------------------
     rm = layer.row_map.long()

@@ -190,9 +190,14 @@ def test_capacity_dropping(factor):
     assert np.array_equal(L.perm_token[:kept].cpu().numpy(), o["perm_token"])
     assert np.array_equal(L.w.bias.cpu().numpy(), o["bias_new"])       # demand drives the bias
     P.assert_close("y_perm (kept rows)", P.np64(L.y_perm[:kept].cpu()), o["y_perm"])
-    y_gather = moe.moe_grouped_swiglu_gather(gi["xn"], L.perm_token, L.offsets, gi["w_gate"], gi["w_up"],
-                                             gi["w_down"])
-    assert torch.equal(y_gather[:kept], L.y_perm[:kept])  # rows gathered from xn: the same bits
+    # the same layer through the permuted copy x_perm: the same bits on the kept rows
+    Lc = moe.MoELayer(moe.LayerWeights(gi["w_router"], gi["bias"].clone(), gi["w_gate"], gi["w_up"],
+                                       gi["w_down"], None), cfg.N, cfg.k, cfg.score_fn, cfg.gamma,
+                      capacity_factor=factor, gather=False)
+    Lc.forward(gi["xn"], gi["h"])
+    torch.cuda.synchronize()
+    assert L.gather and not Lc.gather
+    assert torch.equal(Lc.y_perm[:kept], L.y_perm[:kept])
     P.assert_close("out", P.np64(out.cpu()), o["out"])
     # a token that lost every slot gets exactly its residual back; tokens that kept every
     # slot get the usual bound on the MoE delta (dropping makes the delta's rms over all
