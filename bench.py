@@ -170,7 +170,7 @@ class Step:
                                   cfg.score_fn, cfg.gamma, gather=gather)
         self.ev = None
 
-    def run(self, xn=None, h=None, events=None):
+    def run(self, xn=None, h=None, events=None, out=None):
         L = self.layer
         xn = self.xn if xn is None else xn
         h = self.h if h is None else h
@@ -184,12 +184,12 @@ class Step:
         rec(3)
         L.shared_expert(xn)
         rec(4)
-        L.combine(h)
+        out = L.combine(h, out=out)
         rec(5)
         world = moe.global_counts(L.counts)  # global load histogram for the bias step
         L.bias_step(world)
         rec(6)
-        return L.out
+        return out
 
     @property
     def launches(self):
@@ -221,30 +221,55 @@ def time_device(step, steps, warmup, world):
 
 
 def time_e2e(step, steps, warmup, world):
+    """The layer fed from and drained to pinned host memory every step, the way a serving
+    loop runs it: two sets of device buffers, host-to-device copies of step i+1 and the
+    device-to-host copy of step i-1 on their own streams while step i computes."""
     cfg = step.cfg
     hx = step.xn.cpu().pin_memory()
     hh = step.h.cpu().pin_memory()
-    hout = torch.empty(cfg.N, cfg.D, dtype=step.xn.dtype).pin_memory()
-    dx = torch.empty_like(step.xn)
-    dh = torch.empty_like(step.h)
+    nb = 2
+    hout = [torch.empty(cfg.N, cfg.D, dtype=step.xn.dtype).pin_memory() for _ in range(nb)]
+    dx = [torch.empty_like(step.xn) for _ in range(nb)]
+    dh = [torch.empty_like(step.h) for _ in range(nb)]
+    dout = [torch.empty(cfg.N, cfg.D, dtype=step.xn.dtype, device=step.xn.device) for _ in range(nb)]
+    comp = torch.cuda.current_stream()
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: [torch.cuda.Event() for _ in range(nb)]
+    in_ready, used, out_ready, out_copied = ev(), ev(), ev(), ev()
 
-    def one():
-        dx.copy_(hx, non_blocking=True)
-        dh.copy_(hh, non_blocking=True)
-        out = step.run(dx, dh)
-        hout.copy_(out, non_blocking=True)
+    def run(n):
+        for i in range(n):
+            b = i % nb
+            with torch.cuda.stream(s_in):
+                if i >= nb:
+                    s_in.wait_event(used[b])  # step i-2 no longer reads these inputs
+                dx[b].copy_(hx, non_blocking=True)
+                dh[b].copy_(hh, non_blocking=True)
+                in_ready[b].record(s_in)
+            comp.wait_event(in_ready[b])
+            if i >= nb:
+                comp.wait_event(out_copied[b])  # step i-2's output has reached the host
+            step.run(dx[b], dh[b], out=dout[b])
+            used[b].record(comp)
+            out_ready[b].record(comp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(out_ready[b])
+                hout[b].copy_(dout[b], non_blocking=True)
+                out_copied[b].record(s_out)
+        for b in range(min(n, nb)):
+            comp.wait_event(out_copied[b])
 
-    for _ in range(warmup):
-        one()
+    run(warmup)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    t0.record()
-    for _ in range(steps):
-        one()
-    t1.record()
+    t0.record(comp)
+    s_in.wait_event(t0)
+    s_out.wait_event(t0)
+    run(steps)
+    t1.record(comp)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()

@@ -374,17 +374,17 @@ class MoELayer:
         else:
             self.sh_y = None
 
-    def forward(self, xn, h, update_bias=True, stream=None):
-        """out = h + shared(xn) + sum_j gate_j Expert_j(xn); then the +-gamma bias step."""
-        w = self.w
+    def forward(self, xn, h, update_bias=True, stream=None, out=None):
+        """out = h + shared(xn) + sum_j gate_j Expert_j(xn); then the +-gamma bias step.
+        Writes self.out, or `out` ([N, D], layer dtype) when given, and returns it."""
         self.route(xn, stream)
         self.permute(xn, stream)
         self.experts(xn, stream)
         self.shared_expert(xn, stream)
-        self.combine(h, stream)
+        out = self.combine(h, stream, out)
         if update_bias:
             self.bias_step(1, stream)
-        return self.out
+        return out
 
     def permute(self, xn, stream=None):
         """Histogram, scan, stable permutation (and the row copy unless gathering)."""
@@ -408,9 +408,10 @@ class MoELayer:
             moe_grouped_swiglu(xn, self.sh_offsets, w.shared[0], w.shared[1], w.shared[2],
                                self.sh_h, self.sh_y, stream=stream)
 
-    def combine(self, h, stream=None):
-        moe_unpermute_combine(self.y_perm, self.row_map, self.gate, self.sh_y, h, self.out,
-                              stream=stream)
+    def combine(self, h, stream=None, out=None):
+        out = self.out if out is None else out
+        return moe_unpermute_combine(self.y_perm, self.row_map, self.gate, self.sh_y, h, out,
+                                     stream=stream)
 
     def bias_step(self, replicas=1, stream=None):
         """+-gamma step on this step's counts (summed over `replicas` data-parallel copies)."""
