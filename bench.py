@@ -45,11 +45,12 @@ def peaks():
     return FALLBACK_PEAKS, "fallback"
 
 
-def recorded_traffic(cfg):
-    """ncu DRAM bytes of one grouped SwiGLU call, if recorded for this workload and the kernel
-    sources are unchanged since (else None)."""
+def recorded_traffic(cfg, gather):
+    """ncu DRAM bytes of one grouped SwiGLU call (the row-gathering variant when `gather`), if
+    recorded for this workload and the kernel sources are unchanged since (else None)."""
     import hashlib
-    path = os.path.join(ROOT, "profiles", f"grouped_gemm_{cfg.name}_traffic.txt")
+    suffix = "_gather" if gather else ""
+    path = os.path.join(ROOT, "profiles", f"grouped_gemm_{cfg.name}{suffix}_traffic.txt")
     if not os.path.exists(path):
         return None
     kv = {}
@@ -426,14 +427,17 @@ def main():
                          % (3 * cfg.E * cfg.D * cfg.F * 2 / 1e6),
                    "gemm1_rows": "gathered from xn" if step.layer.gather else "permuted copy x_perm",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "roofline": {"kernel": "moe_grouped_swiglu (GEMM1+SwiGLU and GEMM2 launches)", "bound": "tensor",
+        "roofline": {"kernel": ("moe_grouped_swiglu_gather" if step.layer.gather else "moe_grouped_swiglu")
+                               + " (GEMM1+SwiGLU and GEMM2 launches)", "bound": "tensor",
                      "achieved": gemm_tflops, "peak": peak_t, "unit": "TFLOP/s",
-                     "frac": gemm_tflops / peak_t, "traffic": recorded_traffic(cfg),
+                     "frac": gemm_tflops / peak_t, "traffic": recorded_traffic(cfg, step.layer.gather),
                      "traffic_unit": "bytes per call (ncu)", "peak_kind": peak_label,
                      "frac_of_burst": gemm_tflops / pk["bf16_tflops"]},
         "grouped_gemm_tflops": gemm_tflops,
+        # with gathering, the permute moves no rows (GEMM1 reads them): only its index work
         "permute_gbs": perm_gbs,
-        "permute_frac_hbm": perm_gbs / pk["hbm_gbs"],
+        "permute_frac_hbm": None if step.layer.gather else perm_gbs / pk["hbm_gbs"],
+        "permute_moves_rows": not step.layer.gather,
         "router_gbs": alg["router_bytes"] / (stage_us["router"] * 1e-6) / 1e9,
         "combine_gbs": alg["combine_bytes"] / (stage_us["combine"] * 1e-6) / 1e9,
         "stage_us": {k: round(v, 2) for k, v in stage_us.items()},

@@ -792,6 +792,20 @@ bool make_map_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t col
   return r == CUDA_SUCCESS;
 }
 
+bool make_map_planes_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t planes,
+                          uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {cols, rows, planes};
+  cuuint64_t strides[2] = {cols * 2, rows * cols * 2};
+  cuuint32_t box[3] = {(cuuint32_t)BK, box_rows, planes};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // One tensor map over both projections: planes {gate, up} (or {up, gate} when w_up lies
 // below w_gate; *planes = 2) 'plane distance' bytes apart, so that a 3-D box of
 // (64 columns, box_rows rows, 2 planes) brings the gate and up rows of a tile in one copy.

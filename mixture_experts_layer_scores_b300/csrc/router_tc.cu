@@ -65,7 +65,7 @@ struct Cfg {
   static constexpr int TMEM_COLS = (NBUF + 2) * NT <= 256 ? ((NBUF + 2) * NT <= 128 ? 128 : 256) : 512;
   static constexpr int EPI = NT >= 32 ? 8 : 4;         // epilogue warps
   static constexpr int W = NT / (EPI / 4);             // columns per epilogue thread
-  static constexpr int THREADS = 64 + 32 * EPI;
+  static constexpr int THREADS = 96 + 32 * EPI;       // + warp 2 + EPI: activation copies
   static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES + 512;
 };
 
@@ -124,7 +124,7 @@ router_gemm_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_const
 
   if (t == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full_bar(s), 1);
+      mbar_init(full_bar(s), 2);  // weight-plane copies (warp 0) + activation copies (last warp)
       mbar_init(empty_bar(s), 1);
     }
     for (int a = 0; a < NBUF; ++a) {
@@ -146,18 +146,23 @@ router_gemm_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_const
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
 
-  if (warp == 0) {
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0, issued = 0, issued_par = 0;
+  constexpr int A_WARP = 2 + C::EPI;
+  if ((warp == 0 || warp == A_WARP) && lane == 0) {
+    // warp 0: the three weight planes of the slice as one 3-D box; last warp: the tokens
+    const bool is_w = warp == 0;
+    int stage = 0;
+    uint32_t phase = 0, issued = 0, issued_par = 0;
+    {
       for (int kb = kb0; kb < kb1; ++kb) {
         if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, status, true)) break;
         const uint32_t a_dst = smem_u32(smem + stage * C::STAGE_BYTES);
-        mbar_expect_tx(full_bar(stage), C::STAGE_BYTES);
-        tma_load_2d(a_dst, &map_x, kb * BK, m0, full_bar(stage));
-#pragma unroll
-        for (int sp = 0; sp < 3; ++sp)
-          tma_load_2d(a_dst + C::A_BYTES + sp * C::B_BYTES, &map_w, kb * BK, sp * E + e0, full_bar(stage));
+        if (is_w) {
+          mbar_expect_tx(full_bar(stage), 3 * C::B_BYTES);
+          tma_load_3d(a_dst + C::A_BYTES, &map_w, kb * BK, e0, 0, full_bar(stage));
+        } else {
+          mbar_expect_tx(full_bar(stage), C::A_BYTES);
+          tma_load_2d(a_dst, &map_x, kb * BK, m0, full_bar(stage));
+        }
         issued |= 1u << stage;
         issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -191,7 +196,7 @@ router_gemm_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_const
       tc_commit(done_bar);
       mbar_wait(done_bar, 0, abort_flag, status, false);
     }
-  } else {
+  } else if (warp >= 2 && warp < A_WARP) {
     constexpr int W = C::W;
     const int q = warp & 3;                // TMEM lane quarter
     const int cb = ((warp - 2) >> 2) * W;  // this warp's first column
@@ -392,7 +397,7 @@ extern "C" moe_status_t moe_router_topk_split(const void* xn, int N, int D, cons
   cudaStream_t s = as_cuda(stream);
   CUtensorMap mx, mw;
   if (!tc::make_map_bf16(&mx, xn, (uint64_t)N, (uint64_t)D, rtc::BM) ||
-      !tc::make_map_bf16(&mw, w_split, (uint64_t)3 * E, (uint64_t)D, (uint32_t)p.nt))
+      !tc::make_map_planes_bf16(&mw, w_split, (uint64_t)E, (uint64_t)D, 3, (uint32_t)p.nt))
     return MOE_ERR_CUDA;
   float* part = static_cast<float*>(workspace);
   moe_status_t st =

@@ -253,6 +253,10 @@ __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.
 
 // 2D bf16 row-major [rows, cols] tensor map: box {64 cols, box_rows}, 128-byte swizzle.
 bool make_map_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows);
+// `planes` stacked [rows, cols] bf16 matrices (plane stride rows * cols): a (64, box_rows,
+// planes) box brings the same rows of every plane, plane after plane.
+bool make_map_planes_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t planes,
+                          uint32_t box_rows);
 
 }  // namespace tc
 }  // namespace moe
