@@ -1050,5 +1050,12 @@ extern "C" moe_status_t moe_grouped_swiglu_gather(const void* xn, int N, const i
                        : tc::launch<2>(mg, mg, mu, mho, offsets, G, M_total, D, F, h_workspace, status, s, xn, N,
                                        perm_token);
   if (st != MOE_OK) return st;
+  if (tc::use_pair(G, M_total)) {  // GEMM2 reads H, not gathered rows: CTA pairs as in moe_grouped_swiglu
+    CUtensorMap mh2, mdp;
+    if (!tc::make_map_bf16(&mh2, h_workspace, (uint64_t)M_total, (uint64_t)F, tc::BM / 2) ||
+        !tc::make_map_bf16(&mdp, w_down, (uint64_t)G * D, (uint64_t)F, tc::pair::HB))
+      return MOE_ERR_CUDA;
+    return tc::launch_pair<1>(mh, mh2, mdp, mdp, myo, 0, offsets, G, M_total, F, D, y_perm, status, s);
+  }
   return tc::launch<1>(mh, md, md, myo, offsets, G, M_total, F, D, y_perm, status, s);
 }
