@@ -386,6 +386,24 @@ class MoELayer:
             self.bias_step(1, stream)
         return out
 
+    def capture(self, xn, h, update_bias=True):
+        """Record one forward on the fixed buffers xn and h as a CUDA graph and return a
+        function that replays it (refill xn / h in place between replays).  Every launch of
+        the layer goes through the C ABI on the capture stream; none allocates or waits on the
+        host, so the graph holds exactly the kernels of an eager forward.  For small batches,
+        where launching ten kernels from the host costs more than running them."""
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        # one forward outside the capture (no bias step): the library's one-time set-up per
+        # device happens here, not inside the graph
+        self.forward(xn, h, update_bias=False, stream=s)
+        s.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            self.forward(xn, h, update_bias=update_bias, stream=s)
+        torch.cuda.current_stream().wait_stream(s)
+        return g.replay
+
     def permute(self, xn, stream=None):
         """Histogram, scan, stable permutation (and the row copy unless gathering)."""
         moe_permute(xn, self.idx, self.E, self.counts, self.offsets, self.row_map,

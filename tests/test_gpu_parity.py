@@ -257,3 +257,27 @@ def test_grouped_gemm_pair_and_single_agree(name, monkeypatch):
         got[variant] = g
     assert torch.equal(got["pair"]["y_perm"], got["single"]["y_perm"])
     assert torch.equal(got["pair"]["out"], got["single"]["out"])
+
+
+def test_captured_forward_matches_eager():
+    """A CUDA graph of the whole layer (MoELayer.capture) replays the same kernels: outputs and
+    the evolving bias equal an eager forward's, bit for bit, over several steps."""
+    cfg = synth.scaled(C["handbook"], N=256, D=256, E=16, F=128, k=4)
+    gi = P.make_inputs(cfg, "cuda")
+    mk = lambda: moe.MoELayer(moe.LayerWeights(gi["w_router"], gi["bias"].clone(), gi["w_gate"], gi["w_up"],
+                                               gi["w_down"], None), cfg.N, cfg.k, cfg.score_fn, cfg.gamma)
+    eager, graphed = mk(), mk()
+    xn, h = gi["xn"].clone(), gi["h"].clone()
+    # one eager warm-up call each: the library sets itself up outside the capture
+    eager.forward(xn, h, update_bias=False)
+    graphed.forward(xn, h, update_bias=False)
+    replay = graphed.capture(xn, h)
+    for step in range(3):
+        xn.copy_(gi["xn"] * (1.0 + 0.25 * step))
+        out_e = eager.forward(xn, h).clone()
+        replay()
+        torch.cuda.synchronize()
+        assert moe.last_device_status() == 0
+        assert torch.equal(graphed.out, out_e)
+        assert torch.equal(graphed.w.bias, eager.w.bias)
+        assert torch.equal(graphed.idx, eager.idx)
