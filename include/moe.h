@@ -8,9 +8,13 @@
  *     top_k  = argmax_k(scores + bias)               (bias picks, never weighs)
  *     out    = h + shared(norm(h)) + sum_{e in top_k} gate_e * Expert_e(norm(h))
  *
- * with every expert a SwiGLU FFN.  The five calls below run it step by step:
- * router + top-k + gates, histogram + scan + permute, grouped SwiGLU GEMMs,
- * un-permute + gated combine, and the +-gamma bias step.
+ * with every expert a SwiGLU FFN.  Five steps run it: router + top-k + gates
+ * (moe_router_topk_split after moe_router_split on tensor cores, or moe_router_topk on
+ * CUDA cores), histogram + scan + permute (moe_permute; moe_permute_capacity drops
+ * slots over an expert capacity; moe_permute_noalloc uses library-owned scratch),
+ * grouped SwiGLU GEMMs (moe_grouped_swiglu on permuted rows, or
+ * moe_grouped_swiglu_gather reading the rows through the permutation), un-permute +
+ * gated combine (moe_unpermute_combine), and the +-gamma bias step (moe_bias_update).
  *
  * Conventions shared by every call
  *  - Pointers are DEVICE pointers owned by the caller unless a parameter says
@@ -20,9 +24,12 @@
  *  - Every call is asynchronous on `stream` and returns a moe_status_t.  Host-side
  *    argument checks return MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED before
  *    anything is launched; a launch failure returns MOE_ERR_CUDA.  Faults detected
- *    on the device (a pipeline wait that exceeded its time limit, an expert id out
- *    of range) are recorded in a per-device status word, read by
- *    moe_last_device_status().  No call traps or aborts.
+ *    on the device (a pipeline wait that exceeded its time limit, an expert id or a
+ *    gathered token index out of range) are recorded in a per-device status word,
+ *    read by moe_last_device_status().  No call traps or aborts.
+ *  - No call allocates, synchronises or otherwise waits on the host (except
+ *    moe_last_device_status), so a sequence of calls can be captured in a CUDA graph
+ *    once each entry point has run once on the device.
  *  - Results are deterministic: the same inputs give the same bits, run to run.
  */
 #ifndef MOE_B300_H
