@@ -279,6 +279,43 @@ def time_e2e(step, steps, warmup, world):
     return ms, 2 * cfg.N * cfg.D * b, cfg.N * cfg.D * b
 
 
+def fresh_layer(step, k):
+    """A layer on the step's weights and tokens with the initial bias and k experts per token."""
+    cfg, w = step.cfg, step.layer.w
+    b0 = synth.make_router(cfg, step.dev)[1]
+    return moe.MoELayer(moe.LayerWeights(w.w_router, b0, w.w_gate, w.w_up, w.w_down, w.shared), cfg.N, k,
+                        cfg.score_fn, cfg.gamma)
+
+
+def load_balance_trace(step, steps=50):
+    """max/mean expert load after each of `steps` forwards with the +-gamma bias step, from the
+    initial bias (untimed)."""
+    L = fresh_layer(step, step.cfg.k)
+    trace = []
+    for _ in range(steps):
+        L.forward(step.xn, step.h)
+        trace.append(round(float(L.mom.item()), 4))
+    return {"gamma": step.cfg.gamma, "steps": steps, "max_over_mean_per_step": trace}
+
+
+def time_fewer_experts(step, k, steps, warmup):
+    """The same weights served with k experts per token instead of cfg.k (gates renormalise
+    over the k chosen): tokens/s over `steps` timed forwards."""
+    cfg, xn, h = step.cfg, step.xn, step.h
+    L = fresh_layer(step, k)
+    for _ in range(warmup):
+        L.forward(xn, h)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        L.forward(xn, h)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    return {"k": k, "tokens_per_s": cfg.N / (ms * 1e-3), "ms_per_step": ms}
+
+
 def max_over_ranks(x, world):
     if world == 1:
         return x
@@ -446,6 +483,10 @@ def main():
         "e2e": {"value": tokens / (e2e_ms / args.e2e_steps * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo},
     }
+    if rank == 0:
+        line["load_balance"] = load_balance_trace(step)
+        if cfg.name == "skewed":  # serving with fewer experts per token than trained
+            line["serving_fewer_experts"] = time_fewer_experts(step, 4, min(args.steps, 500), args.warmup)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg)
     if rank == 0:
