@@ -198,27 +198,41 @@ class Step:
 
 
 def time_device(step, steps, warmup, world):
+    """The headline: K forwards + bias steps back to back, with events at the ends only.  On
+    one GPU each step replays a CUDA graph of the layer (MoELayer.capture); with replicas the
+    steps launch eagerly, since the counts all-reduce sits between the forward and the bias
+    step.  Then K more eager steps with events between the stages give the per-stage times
+    (the grouped GEMM's among them, for the roofline).  Returns (ms for the K headline
+    steps, stage µs, launch mode)."""
     for _ in range(warmup):
         step.run()
+    fwd, mode = step.run, "eager"
+    if world == 1:
+        fwd, mode = step.layer.capture(step.xn, step.h), "cuda graph of the layer (MoELayer.capture)"
+        for _ in range(warmup):
+            fwd()
     torch.cuda.synchronize()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(steps)]
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     t0.record()
-    for i in range(steps):
-        step.run(events=evs[i])
+    for _ in range(steps):
+        fwd()
     t1.record()
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     total_ms = t0.elapsed_time(t1)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(steps)]
+    for i in range(steps):
+        step.run(events=evs[i])
+    torch.cuda.synchronize()
     stage_us = {}
     for j, name in enumerate(Step.STAGES):
         stage_us[name] = 1e3 * statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs)
-    return total_ms, stage_us
+    return total_ms, stage_us, mode
 
 
 def time_e2e(step, steps, warmup, world):
@@ -234,6 +248,14 @@ def time_e2e(step, steps, warmup, world):
     dh = [torch.empty_like(step.h) for _ in range(nb)]
     dout = [torch.empty(cfg.N, cfg.D, dtype=step.xn.dtype, device=step.xn.device) for _ in range(nb)]
     comp = torch.cuda.current_stream()
+    for b in range(nb):
+        dx[b].copy_(step.xn)
+        dh[b].copy_(step.h)
+    if world == 1:  # one graph per buffer set, as in the device-timed leg
+        graphs = [step.layer.capture(dx[b], dh[b], out=dout[b]) for b in range(nb)]
+        fwd = lambda b: graphs[b]()
+    else:
+        fwd = lambda b: step.run(dx[b], dh[b], out=dout[b])
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
     ev = lambda: [torch.cuda.Event() for _ in range(nb)]
     in_ready, used, out_ready, out_copied = ev(), ev(), ev(), ev()
@@ -250,7 +272,7 @@ def time_e2e(step, steps, warmup, world):
             comp.wait_event(in_ready[b])
             if i >= nb:
                 comp.wait_event(out_copied[b])  # step i-2's output has reached the host
-            step.run(dx[b], dh[b], out=dout[b])
+            fwd(b)
             used[b].record(comp)
             out_ready[b].record(comp)
             with torch.cuda.stream(s_out):
@@ -305,11 +327,14 @@ def time_fewer_experts(step, k, steps, warmup):
     L = fresh_layer(step, k)
     for _ in range(warmup):
         L.forward(xn, h)
+    fwd = L.capture(xn, h)  # replayed as in the headline leg
+    for _ in range(warmup):
+        fwd()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
     for _ in range(steps):
-        L.forward(xn, h)
+        fwd()
     e1.record()
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
@@ -433,7 +458,7 @@ def main():
     step = Step(cfg, dev, rank, world, gather=True if args.gather else (False if args.permute_copy else None))
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
-        total_ms, stage_us = time_device(step, args.steps, args.warmup, world)
+        total_ms, stage_us, launch_mode = time_device(step, args.steps, args.warmup, world)
     total_ms = max_over_ranks(total_ms, world)
     st = moe.last_device_status()
     if st != 0:
@@ -463,7 +488,9 @@ def main():
                    "l2": "inputs larger than L2: every step streams %.0f MB of expert weights"
                          % (3 * cfg.E * cfg.D * cfg.F * 2 / 1e6),
                    "gemm1_rows": "gathered from xn" if step.layer.gather else "permuted copy x_perm",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "launch": launch_mode,
+                   "stage_us_from": "a second pass of the same steps, eager, events between stages"},
         "roofline": {"kernel": ("moe_grouped_swiglu_gather" if step.layer.gather else "moe_grouped_swiglu")
                                + " (GEMM1+SwiGLU and GEMM2 launches)", "bound": "tensor",
                      "achieved": gemm_tflops, "peak": peak_t, "unit": "TFLOP/s",

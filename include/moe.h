@@ -242,6 +242,19 @@ moe_status_t moe_grouped_swiglu(const void* x_perm, moe_dtype_t dtype, const int
                                 void* y_perm, moe_stream_t stream);
 
 /*
+ * moe_grouped_swiglu_ex -- moe_grouped_swiglu on at most `max_ctas` CTAs (0 = one per
+ * SM).  Same bits as moe_grouped_swiglu for any cap: each CTA walks the tile list with
+ * a stride of the grid size, so a cap only shares the same tiles out among fewer CTAs
+ * (a cap of 1 also rules out the CTA-pair kernel, which needs two).  SMs left over are
+ * free for work on another stream.  MOE_ERR_INVALID_ARG for max_ctas < 0, otherwise the
+ * argument rules and errors of moe_grouped_swiglu.
+ */
+moe_status_t moe_grouped_swiglu_ex(const void* x_perm, moe_dtype_t dtype, const int32_t* offsets,
+                                   int G, int M_total, int D, int F, const void* w_gate,
+                                   const void* w_up, const void* w_down, void* h_workspace,
+                                   void* y_perm, int max_ctas, moe_stream_t stream);
+
+/*
  * moe_grouped_swiglu_gather -- moe_grouped_swiglu with the permutation folded into
  * the first GEMM: row i of expert input is read straight from xn[perm_token[i]], so
  * the permuted copy x_perm is never written.  Same arithmetic as moe_grouped_swiglu

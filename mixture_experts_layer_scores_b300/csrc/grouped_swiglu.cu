@@ -49,6 +49,11 @@ constexpr int STAGING_BYTES = 32 * 128;  // one 32-row x 64-column bf16 output b
 
 constexpr uint32_t IDESC = idesc_bf16(BM, BN);
 
+// Most CTAs a grouped GEMM launch may use (0 = every SM); set for one call by
+// moe_grouped_swiglu_ex so that other work can run on the remaining SMs.
+thread_local int g_max_ctas = 0;
+inline int cta_cap() { return g_max_ctas > 0 ? std::min(g_max_ctas, sm_count()) : sm_count(); }
+
 struct Tile {
   int g, row0, rows, nb, mb;
 };
@@ -846,7 +851,7 @@ moe_status_t launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorM
   const int TN = MODE != 1 ? BN / 2 : BN;
   const long long NB = (NOUT + TN - 1) / TN;
   const long long max_tiles = ((long long)(M_total + BM - 1) / BM + G) * NB;
-  const int grid = (int)std::min<long long>(max_tiles, (long long)sm_count());
+  const int grid = (int)std::min<long long>(max_tiles, (long long)cta_cap());
   kern<<<grid, kThreads<MODE>, smem, s>>>(a, b0, b1, out_map, offsets, G, M_total, K, NOUT,
                                           static_cast<__nv_bfloat16*>(out),
                                           static_cast<const __nv_bfloat16*>(xg), NX, perm, b_planes, nbuf, status);
@@ -870,7 +875,7 @@ moe_status_t launch_pair(const CUtensorMap& a, const CUtensorMap& a_half, const 
   const int TN = MODE == 0 ? BN / 2 : BN;
   const long long NB = (NOUT + TN - 1) / TN;
   const long long max_tiles = ((long long)(M_total + pair::PM - 1) / pair::PM + G) * NB;
-  const int pairs = (int)std::min<long long>(max_tiles, (long long)(sm_count() / 2));
+  const int pairs = (int)std::min<long long>(max_tiles, (long long)(cta_cap() / 2));
   kern<<<2 * pairs, pair::THREADS, smem, s>>>(a, a_half, b, b_up, out_map, offsets, G, M_total, K, NOUT, b_planes,
                                               nbuf, static_cast<__nv_bfloat16*>(out), status);
   return launch_status();
@@ -937,6 +942,7 @@ namespace tc {
 // MOE_GROUPED_GEMM environment variable ("pair", "single", anything else = automatic)
 // overrides the choice.
 bool use_pair(int G, int M_total) {
+  if (cta_cap() < 2) return false;
   const char* e = std::getenv("MOE_GROUPED_GEMM");
   if (e && std::strcmp(e, "pair") == 0) return true;
   if (e && std::strcmp(e, "single") == 0) return false;
@@ -1014,6 +1020,19 @@ extern "C" moe_status_t moe_grouped_swiglu(const void* x_perm, moe_dtype_t dtype
                        : tc::launch<0>(ma, mg, mu, mho, offsets, G, M_total, D, F, h_workspace, status, s);
   if (st != MOE_OK) return st;
   return tc::launch<1>(mh, md, md, myo, offsets, G, M_total, F, D, y_perm, status, s);
+}
+
+extern "C" moe_status_t moe_grouped_swiglu_ex(const void* x_perm, moe_dtype_t dtype, const int32_t* offsets,
+                                              int G, int M_total, int D, int F, const void* w_gate,
+                                              const void* w_up, const void* w_down, void* h_workspace,
+                                              void* y_perm, int max_ctas, moe_stream_t stream) {
+  if (max_ctas < 0) return MOE_ERR_INVALID_ARG;
+  const int saved = moe::tc::g_max_ctas;
+  moe::tc::g_max_ctas = max_ctas;
+  const moe_status_t st = moe_grouped_swiglu(x_perm, dtype, offsets, G, M_total, D, F, w_gate, w_up, w_down,
+                                             h_workspace, y_perm, stream);
+  moe::tc::g_max_ctas = saved;
+  return st;
 }
 
 extern "C" moe_status_t moe_grouped_swiglu_gather(const void* xn, int N, const int32_t* perm_token,

@@ -25,7 +25,7 @@ EXPORTS = ("moe_status_string", "moe_last_device_status", "moe_version", "moe_ro
            "moe_unpermute_combine", "moe_bias_update", "moe_permute_noalloc",
            "moe_permute_noalloc_max_scratch_bytes", "moe_router_split_bytes", "moe_router_split",
            "moe_router_topk_split", "moe_router_topk_split_workspace_bytes", "moe_permute_capacity",
-           "moe_grouped_swiglu_gather")
+           "moe_grouped_swiglu_gather", "moe_grouped_swiglu_ex")
 
 
 class MoEError(RuntimeError):
@@ -55,6 +55,7 @@ def load():
         "moe_permute_workspace_bytes": ([i32, i32, i32], sz),
         "moe_permute": ([vp, i32, i32, i32, vp, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp], i32),
         "moe_grouped_swiglu": ([vp, i32, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp], i32),
+        "moe_grouped_swiglu_ex": ([vp, i32, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, i32, vp], i32),
         "moe_grouped_swiglu_gather": ([vp, i32, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp], i32),
         "moe_unpermute_combine": ([vp, vp, vp, i32, i32, i32, vp, vp, vp, i32, vp], i32),
         "moe_bias_update": ([vp, i32, i64, f32, vp, vp, vp], i32),
@@ -234,8 +235,9 @@ def moe_permute_noalloc(xn, topk_idx, E, counts, offsets, row_map, perm_token, x
 
 
 def moe_grouped_swiglu(x_perm, offsets, w_gate, w_up, w_down, h_workspace=None, y_perm=None,
-                       stream=None):
-    """Grouped SwiGLU over per-group row blocks.  Returns y_perm."""
+                       stream=None, max_ctas=0):
+    """Grouped SwiGLU over per-group row blocks (on at most max_ctas CTAs; 0 = every SM).
+    Returns y_perm."""
     L = load()
     M, D = x_perm.shape
     G, F, _ = w_gate.shape
@@ -244,9 +246,9 @@ def moe_grouped_swiglu(x_perm, offsets, w_gate, w_up, w_down, h_workspace=None, 
     if y_perm is None:
         y_perm = torch.empty(M, D, dtype=x_perm.dtype, device=x_perm.device)
     _cuda(x_perm, offsets, w_gate, w_up, w_down, h_workspace, y_perm)
-    _chk("moe_grouped_swiglu", L.moe_grouped_swiglu(
+    _chk("moe_grouped_swiglu_ex", L.moe_grouped_swiglu_ex(
         _p(x_perm), _dt(x_perm), _p(offsets), G, M, D, F, _p(w_gate), _p(w_up), _p(w_down),
-        _p(h_workspace), _p(y_perm), _stream(stream)))
+        _p(h_workspace), _p(y_perm), int(max_ctas), _stream(stream)))
     return y_perm
 
 
@@ -386,12 +388,14 @@ class MoELayer:
             self.bias_step(1, stream)
         return out
 
-    def capture(self, xn, h, update_bias=True):
-        """Record one forward on the fixed buffers xn and h as a CUDA graph and return a
-        function that replays it (refill xn / h in place between replays).  Every launch of
-        the layer goes through the C ABI on the capture stream; none allocates or waits on the
-        host, so the graph holds exactly the kernels of an eager forward.  For small batches,
-        where launching ten kernels from the host costs more than running them."""
+    def capture(self, xn, h, update_bias=True, out=None):
+        """Record one forward on the fixed buffers xn and h (writing self.out, or `out`) as a
+        CUDA graph and return a function that replays it on the current stream (refill xn / h
+        in place between replays).  Every launch of the layer goes through the C ABI on the
+        capture stream; none allocates or waits on the host, so the graph holds exactly the
+        kernels of an eager forward.  Replays leave out the host's launch work and most of
+        the device's gaps between dependent launches: about 1.5 % of a forward at N=8192,
+        D=2048, E=64, F=1024, and most of it for small batches."""
         s = torch.cuda.Stream()
         s.wait_stream(torch.cuda.current_stream())
         # one forward outside the capture (no bias step): the library's one-time set-up per
@@ -400,7 +404,7 @@ class MoELayer:
         s.synchronize()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=s):
-            self.forward(xn, h, update_bias=update_bias, stream=s)
+            self.forward(xn, h, update_bias=update_bias, stream=s, out=out)
         torch.cuda.current_stream().wait_stream(s)
         return g.replay
 

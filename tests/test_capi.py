@@ -83,6 +83,13 @@ def test_host_validation_rejects_before_launch(lib):
                                          vp(16), vp(16), vp(16), None) == -1
     assert lib.moe_grouped_swiglu_gather(None, 0, None, None, 4, 0, 128, 128, None, None, None, None,
                                          None, None) == 0
+    # capped GEMM: negative cap; the cap changes nothing about the shape rules or the no-op
+    assert lib.moe_grouped_swiglu_ex(vp(16), 1, vp(16), 4, 100, 128, 128, vp(16), vp(16), vp(16), vp(16),
+                                     vp(16), -1, None) == -1
+    assert lib.moe_grouped_swiglu_ex(vp(16), 1, vp(16), 4, 100, 128, 96, vp(16), vp(16), vp(16), vp(16),
+                                     vp(16), 8, None) == -2
+    assert lib.moe_grouped_swiglu_ex(None, 1, None, 4, 0, 128, 128, None, None, None, None, None, 8,
+                                     None) == 0
     # combine: k too large; bias: null counts
     assert lib.moe_unpermute_combine(vp(16), vp(16), vp(16), 4, 17, 64, None, None, vp(16), 1, None) == -2
     assert lib.moe_bias_update(None, 8, 64, ctypes.c_float(1e-3), vp(16), None, None) == -1

@@ -259,6 +259,29 @@ def test_grouped_gemm_pair_and_single_agree(name, monkeypatch):
     assert torch.equal(got["pair"]["out"], got["single"]["out"])
 
 
+@pytest.mark.parametrize("name", ["pair_ragged_F384", "pair_with_empty_experts"])
+def test_grouped_gemm_cta_cap_keeps_bits(name):
+    """moe_grouped_swiglu_ex on 1, 2, 3 or 20 CTAs writes the same H and Y bits as on every
+    SM: the cap only deals the same tiles out among fewer CTAs."""
+    cfg = PAIR_CASES[name]
+    gi = P.make_inputs(cfg, "cuda")
+    g = P.gpu_layer(cfg, gi)
+    x_perm, offsets = g["x_perm"].cuda(), g["offsets"].cuda()
+    M, F = x_perm.shape[0], gi["w_gate"].shape[1]
+    ref = None
+    for cap in (0, 1, 2, 3, 20):
+        h_ws = torch.full((M, F), float("nan"), dtype=torch.bfloat16, device="cuda")
+        y = moe.moe_grouped_swiglu(x_perm, offsets, gi["w_gate"], gi["w_up"], gi["w_down"], h_ws,
+                                   max_ctas=cap)
+        torch.cuda.synchronize()
+        assert moe.last_device_status() == 0
+        if ref is None:
+            ref = (h_ws.clone(), y.clone())
+            assert torch.equal(y.cpu(), g["y_perm"])
+        else:
+            assert torch.equal(h_ws, ref[0]) and torch.equal(y, ref[1]), cap
+
+
 def test_captured_forward_matches_eager():
     """A CUDA graph of the whole layer (MoELayer.capture) replays the same kernels: outputs and
     the evolving bias equal an eager forward's, bit for bit, over several steps."""
