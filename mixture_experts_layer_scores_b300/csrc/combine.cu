@@ -5,6 +5,7 @@
 // "Load-balancing problem" item 3 and "Build it" step 2: each expert's bias moves by
 // gamma against the sign of its load error.
 #include "moe_internal.cuh"
+#include "tc_common.cuh"
 
 namespace moe {
 namespace {
@@ -18,6 +19,9 @@ struct Vec<__nv_bfloat16> {
   __device__ static void load(const void* p, float* f) {
     bf16x8_to_f32(__ldg(static_cast<const uint4*>(p)), f);
   }
+  __device__ static void load_shared(const void* p, float* f) {
+    bf16x8_to_f32(*static_cast<const uint4*>(p), f);
+  }
   __device__ static void store(void* p, const float* f) {
     *static_cast<uint4*>(p) = f32_to_bf16x8(f);
   }
@@ -30,54 +34,80 @@ struct Vec<float> {
     const float4 v = __ldg(static_cast<const float4*>(p));
     f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
   }
+  __device__ static void load_shared(const void* p, float* f) {
+    const float4 v = *static_cast<const float4*>(p);
+    f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
+  }
   __device__ static void store(void* p, const float* f) {
     *static_cast<float4*>(p) = make_float4(f[0], f[1], f[2], f[3]);
   }
 };
 
-// One block per token; threads stride over the row's 16-byte vectors.
+// One CTA per (token, column chunk of CHB bytes); thread i owns the chunk's 16-byte vector i.
+// Each thread starts async copies (cp.async, L2 only) of its vector from the token's k
+// expert rows and its shared-expert and residual rows into shared memory, waits for its own
+// copies, then weights and sums them in slot order and writes out.  The copies keep k + 2
+// loads per thread in flight without holding registers for them, and at 20 KB of shared
+// memory per CTA (k = 8) about ten CTAs share an SM: enough requests in flight to keep
+// HBM busy, which a loop of dependent register loads over j is not.
+constexpr int CHB = 2048;
+constexpr int THREADS = CHB / 16;
+
 template <typename T>
-__global__ void __launch_bounds__(128) combine_kernel(const T* __restrict__ y, const int32_t* __restrict__ row_map,
-                                                      const float* __restrict__ gate, int k, int D,
-                                                      const T* __restrict__ shared_y,
-                                                      const T* __restrict__ residual, T* __restrict__ out) {
+__global__ void __launch_bounds__(THREADS) combine_kernel(const T* __restrict__ y, const int32_t* __restrict__ row_map,
+                                                          const float* __restrict__ gate, int k, int D,
+                                                          const T* __restrict__ shared_y,
+                                                          const T* __restrict__ residual, T* __restrict__ out) {
+  using namespace tc;
   constexpr int W = Vec<T>::W;
-  const int n = blockIdx.x;
+  extern __shared__ __align__(16) uint8_t stage[];  // [k + 2][CHB]: expert rows, shared, residual
   __shared__ int rows[MOE_MAX_TOPK];
   __shared__ float gs[MOE_MAX_TOPK];
+  const int rowbytes = D * (int)sizeof(T);
+  const int nch = (rowbytes + CHB - 1) / CHB;
+  const int n = blockIdx.x / nch, c = blockIdx.x % nch;
   if (threadIdx.x < k) {
     rows[threadIdx.x] = row_map[(size_t)n * k + threadIdx.x];
     gs[threadIdx.x] = gate[(size_t)n * k + threadIdx.x];
   }
   __syncthreads();
-  const int V = D / W;
-  for (int c = threadIdx.x; c < V; c += blockDim.x) {
-    float acc[W];
+  const int off = c * CHB + threadIdx.x * 16;
+  if (off >= rowbytes) return;
+  const uint32_t mine = smem_u32(stage) + threadIdx.x * 16;
+  const uint8_t* yb = reinterpret_cast<const uint8_t*>(y);
+  for (int j = 0; j < k; ++j)
+    if (rows[j] >= 0) cp_async_16(mine + j * CHB, yb + (size_t)rows[j] * rowbytes + off, 16);
+  if (shared_y)
+    cp_async_16(mine + k * CHB, reinterpret_cast<const uint8_t*>(shared_y) + (size_t)n * rowbytes + off, 16);
+  if (residual)
+    cp_async_16(mine + (k + 1) * CHB, reinterpret_cast<const uint8_t*>(residual) + (size_t)n * rowbytes + off, 16);
+  cp_async_commit();
+  cp_async_wait<0>();
+  const uint8_t* v = stage + threadIdx.x * 16;
+  float acc[W];
 #pragma unroll
-    for (int i = 0; i < W; ++i) acc[i] = 0.f;
-    for (int j = 0; j < k; ++j) {
-      const int r = rows[j];
-      if (r < 0) continue;
-      float f[W];
-      Vec<T>::load(y + (size_t)r * D + c * W, f);
-      const float g = gs[j];
+  for (int i = 0; i < W; ++i) acc[i] = 0.f;
+  for (int j = 0; j < k; ++j) {
+    if (rows[j] < 0) continue;  // dropped slot
+    float f[W];
+    Vec<T>::load_shared(v + j * CHB, f);
+    const float g = gs[j];
 #pragma unroll
-      for (int i = 0; i < W; ++i) acc[i] = fmaf(g, f[i], acc[i]);
-    }
-    if (shared_y) {
-      float f[W];
-      Vec<T>::load(shared_y + (size_t)n * D + c * W, f);
-#pragma unroll
-      for (int i = 0; i < W; ++i) acc[i] += f[i];
-    }
-    if (residual) {
-      float f[W];
-      Vec<T>::load(residual + (size_t)n * D + c * W, f);
-#pragma unroll
-      for (int i = 0; i < W; ++i) acc[i] += f[i];
-    }
-    Vec<T>::store(out + (size_t)n * D + c * W, acc);
+    for (int i = 0; i < W; ++i) acc[i] = fmaf(g, f[i], acc[i]);
   }
+  if (shared_y) {
+    float f[W];
+    Vec<T>::load_shared(v + k * CHB, f);
+#pragma unroll
+    for (int i = 0; i < W; ++i) acc[i] += f[i];
+  }
+  if (residual) {
+    float f[W];
+    Vec<T>::load_shared(v + (k + 1) * CHB, f);
+#pragma unroll
+    for (int i = 0; i < W; ++i) acc[i] += f[i];
+  }
+  Vec<T>::store(reinterpret_cast<uint8_t*>(out) + (size_t)n * rowbytes + off, acc);
 }
 
 __global__ void bias_update_kernel(const int32_t* __restrict__ counts, int E, long long total,
@@ -121,16 +151,19 @@ extern "C" moe_status_t moe_unpermute_combine(const void* y_perm, const int32_t*
   if (!aligned16(y_perm) || !aligned16(out) || (shared_y && !aligned16(shared_y)) ||
       (residual && !aligned16(residual)))
     return MOE_ERR_INVALID_ARG;
+  const long long blocks = (long long)N * ((D * esize + CHB - 1) / CHB);
+  if (blocks > 0x7fffffffll) return MOE_ERR_UNSUPPORTED;
   cudaStream_t s = as_cuda(stream);
+  const size_t smem = (size_t)(k + 2) * CHB;  // at most 36 KB: no opt-in needed
   if (dtype == MOE_BF16)
-    combine_kernel<__nv_bfloat16><<<N, 128, 0, s>>>(
+    combine_kernel<__nv_bfloat16><<<(unsigned)blocks, THREADS, smem, s>>>(
         static_cast<const __nv_bfloat16*>(y_perm), row_map, topk_gate, k, D,
         static_cast<const __nv_bfloat16*>(shared_y), static_cast<const __nv_bfloat16*>(residual),
         static_cast<__nv_bfloat16*>(out));
   else
-    combine_kernel<float><<<N, 128, 0, s>>>(static_cast<const float*>(y_perm), row_map, topk_gate, k, D,
-                                            static_cast<const float*>(shared_y),
-                                            static_cast<const float*>(residual), static_cast<float*>(out));
+    combine_kernel<float><<<(unsigned)blocks, THREADS, smem, s>>>(
+        static_cast<const float*>(y_perm), row_map, topk_gate, k, D, static_cast<const float*>(shared_y),
+        static_cast<const float*>(residual), static_cast<float*>(out));
   return launch_status();
 }
 

@@ -304,3 +304,37 @@ def test_captured_forward_matches_eager():
         assert torch.equal(graphed.out, out_e)
         assert torch.equal(graphed.w.bias, eager.w.bias)
         assert torch.equal(graphed.idx, eager.idx)
+
+
+COMBINE_CASES = {
+    # (dtype, N, D, k, shared, residual): rows of 2688 / 2800 / 14336 bytes cross 2 KB column
+    # chunks with a ragged last one; a 128-byte row, k = 16, and a single token
+    "bf16_D1344_k8_shared_residual": (torch.bfloat16, 700, 1344, 8, True, True),
+    "f32_D700_k3_residual": (torch.float32, 301, 700, 3, False, True),
+    "bf16_D64_k16_bare": (torch.bfloat16, 149, 64, 16, False, False),
+    "bf16_D7168_k8_shared": (torch.bfloat16, 40, 7168, 8, True, False),
+    "bf16_single_token": (torch.bfloat16, 1, 2048, 4, True, True),
+}
+
+
+@pytest.mark.parametrize("name", list(COMBINE_CASES))
+def test_combine_chunks_and_dropped_slots(name):
+    """moe_unpermute_combine against the oracle's combine on rows that span several column
+    chunks (with a ragged last chunk), with about 10 % of the slots dropped (row -1)."""
+    dt, N, D, k, with_shared, with_res = COMBINE_CASES[name]
+    g = torch.Generator().manual_seed(N * 131 + D)
+    M = N * k
+    y_perm = torch.randn(M, D, generator=g).to(dt)
+    row_map = torch.randperm(M, generator=g).to(torch.int32).reshape(N, k)
+    row_map[torch.rand(N, k, generator=g) < 0.1] = -1
+    gate = torch.rand(N, k, generator=g)
+    shared = torch.randn(N, D, generator=g).to(dt) if with_shared else None
+    res = torch.randn(N, D, generator=g).to(dt) if with_res else None
+    cu = lambda t: None if t is None else t.cuda()
+    out = moe.moe_unpermute_combine(cu(y_perm), cu(row_map), cu(gate), cu(shared), cu(res))
+    torch.cuda.synchronize()
+    assert moe.last_device_status() == 0
+    ref = moe_oracle.combine(P.np64(y_perm), row_map.numpy(), gate.numpy().astype(np.float64),
+                             residual=None if res is None else P.np64(res),
+                             shared_y=None if shared is None else P.np64(shared))
+    P.assert_close(name, P.np64(out.cpu()), ref, f32=dt == torch.float32)
