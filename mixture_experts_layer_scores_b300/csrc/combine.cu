@@ -66,6 +66,8 @@ __global__ void __launch_bounds__(THREADS) combine_kernel(const T* __restrict__ 
   const int rowbytes = D * (int)sizeof(T);
   const int nch = (rowbytes + CHB - 1) / CHB;
   const int n = blockIdx.x / nch, c = blockIdx.x % nch;
+  grid_dep_wait();
+  grid_dep_launch();
   if (threadIdx.x < k) {
     rows[threadIdx.x] = row_map[(size_t)n * k + threadIdx.x];
     gs[threadIdx.x] = gate[(size_t)n * k + threadIdx.x];
@@ -113,6 +115,8 @@ __global__ void __launch_bounds__(THREADS) combine_kernel(const T* __restrict__ 
 __global__ void bias_update_kernel(const int32_t* __restrict__ counts, int E, long long total,
                                    float gamma, float* __restrict__ bias, float* __restrict__ mom) {
   __shared__ int smax[32];
+  grid_dep_wait();
+  grid_dep_launch();
   int m = 0;
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     const long long c = counts[e];
@@ -156,15 +160,13 @@ extern "C" moe_status_t moe_unpermute_combine(const void* y_perm, const int32_t*
   cudaStream_t s = as_cuda(stream);
   const size_t smem = (size_t)(k + 2) * CHB;  // at most 36 KB: no opt-in needed
   if (dtype == MOE_BF16)
-    combine_kernel<__nv_bfloat16><<<(unsigned)blocks, THREADS, smem, s>>>(
-        static_cast<const __nv_bfloat16*>(y_perm), row_map, topk_gate, k, D,
-        static_cast<const __nv_bfloat16*>(shared_y), static_cast<const __nv_bfloat16*>(residual),
-        static_cast<__nv_bfloat16*>(out));
-  else
-    combine_kernel<float><<<(unsigned)blocks, THREADS, smem, s>>>(
-        static_cast<const float*>(y_perm), row_map, topk_gate, k, D, static_cast<const float*>(shared_y),
-        static_cast<const float*>(residual), static_cast<float*>(out));
-  return launch_status();
+    return launch_kernel(combine_kernel<__nv_bfloat16>, dim3((unsigned)blocks), dim3(THREADS), smem, s,
+                         static_cast<const __nv_bfloat16*>(y_perm), row_map, topk_gate, k, D,
+                         static_cast<const __nv_bfloat16*>(shared_y), static_cast<const __nv_bfloat16*>(residual),
+                         static_cast<__nv_bfloat16*>(out));
+  return launch_kernel(combine_kernel<float>, dim3((unsigned)blocks), dim3(THREADS), smem, s,
+                       static_cast<const float*>(y_perm), row_map, topk_gate, k, D, static_cast<const float*>(shared_y),
+                       static_cast<const float*>(residual), static_cast<float*>(out));
 }
 
 extern "C" moe_status_t moe_bias_update(const int32_t* counts, int E, int64_t total_assignments,
@@ -173,7 +175,6 @@ extern "C" moe_status_t moe_bias_update(const int32_t* counts, int E, int64_t to
   using namespace moe;
   if (E < 1 || total_assignments < 0 || !counts || !bias) return MOE_ERR_INVALID_ARG;
   if (E > 1 << 20) return MOE_ERR_UNSUPPORTED;
-  bias_update_kernel<<<1, 1024, 0, as_cuda(stream)>>>(counts, E, (long long)total_assignments, gamma,
-                                                      bias, max_over_mean_out);
-  return launch_status();
+  return launch_kernel(bias_update_kernel, dim3(1), dim3(1024), 0, as_cuda(stream), counts, E,
+                       (long long)total_assignments, gamma, bias, max_over_mean_out);
 }

@@ -159,6 +159,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
     if (SWIGLU) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_b1)) : "memory");
   }
 
+  grid_dep_wait();  // set-up done; the offsets and operands come from earlier kernels
+  grid_dep_launch();
+
   // tile_start[g] = sum over g' < g of (row blocks of g') * NB
   {
     const int per = (G + NTHR - 1) / NTHR;
@@ -537,6 +540,9 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_a_half)) : "memory");
   }
 
+  grid_dep_wait();  // set-up done; the offsets and operands come from earlier kernels
+  grid_dep_launch();
+
   // tile_start[g] = sum over g' < g of (256-row blocks of g') * NB
   {
     const int per = (G + pair::THREADS - 1) / pair::THREADS;
@@ -852,10 +858,9 @@ moe_status_t launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorM
   const long long NB = (NOUT + TN - 1) / TN;
   const long long max_tiles = ((long long)(M_total + BM - 1) / BM + G) * NB;
   const int grid = (int)std::min<long long>(max_tiles, (long long)cta_cap());
-  kern<<<grid, kThreads<MODE>, smem, s>>>(a, b0, b1, out_map, offsets, G, M_total, K, NOUT,
-                                          static_cast<__nv_bfloat16*>(out),
-                                          static_cast<const __nv_bfloat16*>(xg), NX, perm, b_planes, nbuf, status);
-  return launch_status();
+  return launch_kernel(kern, dim3(grid), dim3(kThreads<MODE>), smem, s, a, b0, b1, out_map, offsets, G, M_total, K,
+                       NOUT, static_cast<__nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(xg), NX, perm,
+                       b_planes, nbuf, status);
 }
 
 size_t pair_smem_bytes(int G, int nbuf) {
@@ -876,9 +881,8 @@ moe_status_t launch_pair(const CUtensorMap& a, const CUtensorMap& a_half, const 
   const long long NB = (NOUT + TN - 1) / TN;
   const long long max_tiles = ((long long)(M_total + pair::PM - 1) / pair::PM + G) * NB;
   const int pairs = (int)std::min<long long>(max_tiles, (long long)(cta_cap() / 2));
-  kern<<<2 * pairs, pair::THREADS, smem, s>>>(a, a_half, b, b_up, out_map, offsets, G, M_total, K, NOUT, b_planes,
-                                              nbuf, static_cast<__nv_bfloat16*>(out), status);
-  return launch_status();
+  return launch_kernel(kern, dim3(2 * pairs), dim3(pair::THREADS), smem, s, a, a_half, b, b_up, out_map, offsets, G,
+                       M_total, K, NOUT, b_planes, nbuf, static_cast<__nv_bfloat16*>(out), status);
 }
 
 }  // namespace tc
@@ -888,6 +892,8 @@ namespace simt {
 __global__ void swiglu_up_kernel(const float* __restrict__ x, const int32_t* __restrict__ offsets, int G,
                                  int M, int D, int F, const float* __restrict__ wg,
                                  const float* __restrict__ wu, float* __restrict__ h) {
+  grid_dep_wait();
+  grid_dep_launch();
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (long long)M * F) return;
   const int r = (int)(i / F), f = (int)(i % F);
@@ -913,6 +919,8 @@ __global__ void swiglu_up_kernel(const float* __restrict__ x, const int32_t* __r
 
 __global__ void swiglu_down_kernel(const float* __restrict__ h, const int32_t* __restrict__ offsets, int G,
                                    int M, int D, int F, const float* __restrict__ wd, float* __restrict__ y) {
+  grid_dep_wait();
+  grid_dep_launch();
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (long long)M * D) return;
   const int r = (int)(i / D), d = (int)(i % D);
@@ -970,13 +978,14 @@ extern "C" moe_status_t moe_grouped_swiglu(const void* x_perm, moe_dtype_t dtype
   if (dtype == MOE_F32) {
     const int T = 256;
     const long long n1 = (long long)M_total * F, n2 = (long long)M_total * D;
-    simt::swiglu_up_kernel<<<(unsigned)((n1 + T - 1) / T), T, 0, s>>>(
-        static_cast<const float*>(x_perm), offsets, G, M_total, D, F, static_cast<const float*>(w_gate),
-        static_cast<const float*>(w_up), static_cast<float*>(h_workspace));
-    simt::swiglu_down_kernel<<<(unsigned)((n2 + T - 1) / T), T, 0, s>>>(
-        static_cast<const float*>(h_workspace), offsets, G, M_total, D, F, static_cast<const float*>(w_down),
-        static_cast<float*>(y_perm));
-    return launch_status();
+    const moe_status_t st = launch_kernel(
+        simt::swiglu_up_kernel, dim3((unsigned)((n1 + T - 1) / T)), dim3(T), 0, s, static_cast<const float*>(x_perm),
+        offsets, G, M_total, D, F, static_cast<const float*>(w_gate), static_cast<const float*>(w_up),
+        static_cast<float*>(h_workspace));
+    if (st != MOE_OK) return st;
+    return launch_kernel(simt::swiglu_down_kernel, dim3((unsigned)((n2 + T - 1) / T)), dim3(T), 0, s,
+                         static_cast<const float*>(h_workspace), offsets, G, M_total, D, F,
+                         static_cast<const float*>(w_down), static_cast<float*>(y_perm));
   }
   int* status = device_status_word();
   if (!status) return MOE_ERR_CUDA;

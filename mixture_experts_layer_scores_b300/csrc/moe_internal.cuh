@@ -5,6 +5,9 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <cstdlib>
+#include <utility>
+
 #include "../../include/moe.h"
 
 namespace moe {
@@ -23,6 +26,46 @@ inline moe_status_t launch_status() {
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
+
+// ---- launches ---------------------------------------------------------------------------
+//
+// Every kernel of the library is launched with programmatic stream serialization: it may
+// start (launch its CTAs, set up barriers and tensor memory) while the kernel before it on
+// the stream is still draining.  Each kernel calls grid_dep_wait() before its first access
+// to global memory that another kernel writes or reads, which returns once the preceding
+// kernel has completed and its writes are visible, and then grid_dep_launch(), which lets
+// the next kernel start launching in turn.  MOE_PDL=0 in the environment launches plainly.
+
+inline bool pdl_enabled() {
+  static const bool on = [] {
+    const char* e = std::getenv("MOE_PDL");
+    return !(e && e[0] == '0');
+  }();
+  return on;
+}
+
+template <typename... KArgs, typename... Args>
+inline moe_status_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                  Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  if (cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  return launch_status();
+}
+
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 inline int sm_count() {
   int dev = 0, n = 0;

@@ -41,6 +41,8 @@ __global__ void __launch_bounds__(256) hist_kernel(const int32_t* __restrict__ i
                                                    int* __restrict__ status) {
   extern __shared__ int sh[];
   for (int e = threadIdx.x; e < E; e += blockDim.x) sh[e] = 0;
+  grid_dep_wait();
+  grid_dep_launch();
   __syncthreads();
   const int s0 = blockIdx.x * C, s1 = min(R, s0 + C);
   bool bad = false;
@@ -67,6 +69,8 @@ __global__ void __launch_bounds__(1024) scan_kernel(int32_t* __restrict__ ws, in
   const int g = t / E, e = t % E;
   const int per = (nb + P - 1) / P;
   const int b0 = g * per, b1 = min(nb, b0 + per);
+  grid_dep_wait();
+  grid_dep_launch();
   if (g < P) {
     int sum = 0;
     for (int b = b0; b < b1; ++b) sum += ws[(size_t)b * E + e];
@@ -129,6 +133,8 @@ __global__ void __launch_bounds__(256) rank_kernel(const int32_t* __restrict__ i
   int* running = sh;          // [E]
   int* wcnt = sh + E;         // [8][E]
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  grid_dep_wait();
+  grid_dep_launch();
   for (int e = t; e < E; e += 256) {
     running[e] = ws[(size_t)blockIdx.x * E + e];
 #pragma unroll
@@ -181,6 +187,8 @@ __global__ void __launch_bounds__(256) copy_kernel(const uint4* __restrict__ xn,
                                                    const int32_t* __restrict__ row_map,
                                                    uint4* __restrict__ x_perm) {
   constexpr int U = 4;
+  grid_dep_wait();
+  grid_dep_launch();
   const long long total = (long long)N * V;
   const long long stride = (long long)gridDim.x * blockDim.x;
   for (long long i0 = (long long)blockIdx.x * blockDim.x + threadIdx.x; i0 < total; i0 += stride * U) {
@@ -241,13 +249,18 @@ extern "C" moe_status_t moe_permute_capacity(const void* xn, moe_dtype_t dtype, 
   const Plan p = plan(N);
   const int R = N * k, C = p.tpb * k;
   int32_t* ws = static_cast<int32_t*>(workspace);
-  hist_kernel<<<p.nb, 256, E * sizeof(int), s>>>(topk_idx, R, E, C, ws, status);
+  moe_status_t st = launch_kernel(hist_kernel, dim3(p.nb), dim3(256), E * sizeof(int), s, topk_idx, R, E, C, ws,
+                                  status);
+  if (st != MOE_OK) return st;
   const int P = 1024 / E;
-  scan_kernel<<<1, 1024, (size_t)(P * E + E + 32) * sizeof(int), s>>>(ws, p.nb, E, capacity, counts,
-                                                                        offsets);
+  st = launch_kernel(scan_kernel, dim3(1), dim3(1024), (size_t)(P * E + E + 32) * sizeof(int), s, ws, p.nb, E,
+                     capacity, counts, offsets);
+  if (st != MOE_OK) return st;
   if (row_map) {
-    rank_kernel<<<p.nb, 256, (size_t)9 * E * sizeof(int), s>>>(topk_idx, R, k, E, C, capacity, ws, offsets,
-                                                                row_map, perm_token);
+    st = launch_kernel(rank_kernel, dim3(p.nb), dim3(256), (size_t)9 * E * sizeof(int), s, topk_idx, R, k, E, C,
+                       capacity, static_cast<const int32_t*>(ws), static_cast<const int32_t*>(offsets), row_map,
+                       perm_token);
+    if (st != MOE_OK) return st;
   }
   if (x_perm) {
     const int V = (int)(D * esize / 16);
@@ -255,10 +268,10 @@ extern "C" moe_status_t moe_permute_capacity(const void* xn, moe_dtype_t dtype, 
     long long blocks = (items + 256 * 4 - 1) / (256 * 4);
     const long long cap = (long long)sm_count() * 8;
     if (blocks > cap) blocks = cap;
-    copy_kernel<<<(int)blocks, 256, 0, s>>>(static_cast<const uint4*>(xn), N, V, k, row_map,
-                                            static_cast<uint4*>(x_perm));
+    return launch_kernel(copy_kernel, dim3((unsigned)blocks), dim3(256), 0, s, static_cast<const uint4*>(xn), N, V, k,
+                         static_cast<const int32_t*>(row_map), static_cast<uint4*>(x_perm));
   }
-  return launch_status();
+  return MOE_OK;
 }
 
 extern "C" moe_status_t moe_permute(const void* xn, moe_dtype_t dtype, int N, int D,

@@ -40,6 +40,8 @@ constexpr int UK = 16;
 
 __global__ void split_kernel(const float* __restrict__ w, long long n, __nv_bfloat16* __restrict__ out) {
   const long long stride = (long long)gridDim.x * blockDim.x;
+  grid_dep_wait();
+  grid_dep_launch();
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
     const float x = w[i];
     const __nv_bfloat16 hi = __float2bfloat16_rn(x);
@@ -145,6 +147,8 @@ router_gemm_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_const
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
+  grid_dep_wait();  // barriers and tensor memory are set up; from here on the inputs are read
+  grid_dep_launch();
 
   constexpr int A_WARP = 2 + C::EPI;
   if ((warp == 0 || warp == A_WARP) && lane == 0) {
@@ -294,6 +298,8 @@ __global__ void __launch_bounds__(256) topk_kernel(float* __restrict__ logits, c
                                                    uint8_t* __restrict__ tie) {
   const int lane = threadIdx.x & 31;
   const int n = blockIdx.x * 8 + (threadIdx.x >> 5);
+  grid_dep_wait();
+  grid_dep_launch();
   if (n >= N) return;
   float* row = logits + (size_t)n * E;
   float lg[PER];
@@ -332,8 +338,8 @@ moe_status_t launch_gemm(const CUtensorMap& mx, const CUtensorMap& mw, int N, in
   const int KB = D / BK;
   const int per = (KB + nsplit - 1) / nsplit;
   dim3 grid((N + BM - 1) / BM, (E + NT - 1) / NT, nsplit);
-  kern<<<grid, Cfg<NT>::THREADS, Cfg<NT>::SMEM, s>>>(mx, mw, N, D, E, per, logits, partials, status);
-  return launch_status();
+  return launch_kernel(kern, grid, dim3(Cfg<NT>::THREADS), Cfg<NT>::SMEM, s, mx, mw, N, D, E, per, logits, partials,
+                       status);
 }
 
 // Tile width and split-K count for (N, D, E): about 128 CTAs, at most 4 splits.
@@ -367,8 +373,8 @@ extern "C" moe_status_t moe_router_split(const float* w_router, int E, int D, vo
   if (E < 1 || D < 1 || !w_router || !w_split) return MOE_ERR_INVALID_ARG;
   const long long n = (long long)E * D;
   const int blocks = (int)std::min<long long>((n + 255) / 256, (long long)sm_count() * 8);
-  rtc::split_kernel<<<blocks, 256, 0, as_cuda(stream)>>>(w_router, n, static_cast<__nv_bfloat16*>(w_split));
-  return launch_status();
+  return launch_kernel(rtc::split_kernel, dim3(blocks), dim3(256), 0, as_cuda(stream), w_router, n,
+                       static_cast<__nv_bfloat16*>(w_split));
 }
 
 extern "C" size_t moe_router_topk_split_workspace_bytes(int N, int D, int E) {
@@ -407,14 +413,14 @@ extern "C" moe_status_t moe_router_topk_split(const void* xn, int N, int D, cons
   if (st != MOE_OK) return st;
   const int sig = (int)fn;  // score function code
   const int grid = (N + 7) / 8;
-#define MOE_TOPK(PER) rtc::topk_kernel<PER><<<grid, 256, 0, s>>>(logits_out, part, p.nsplit, bias, N, E, k, sig, \
-                                                                 topk_idx, topk_gate, near_tie)
-  if (E <= 32) MOE_TOPK(1);
-  else if (E <= 64) MOE_TOPK(2);
-  else if (E <= 128) MOE_TOPK(4);
-  else if (E <= 256) MOE_TOPK(8);
-  else if (E <= 512) MOE_TOPK(16);
-  else MOE_TOPK(32);
-#undef MOE_TOPK
-  return launch_status();
+  auto topk = [&](auto kern) {
+    return launch_kernel(kern, dim3(grid), dim3(256), 0, s, logits_out, static_cast<const float*>(part), p.nsplit,
+                         bias, N, E, k, sig, topk_idx, topk_gate, near_tie);
+  };
+  if (E <= 32) return topk(rtc::topk_kernel<1>);
+  if (E <= 64) return topk(rtc::topk_kernel<2>);
+  if (E <= 128) return topk(rtc::topk_kernel<4>);
+  if (E <= 256) return topk(rtc::topk_kernel<8>);
+  if (E <= 512) return topk(rtc::topk_kernel<16>);
+  return topk(rtc::topk_kernel<32>);
 }

@@ -105,6 +105,8 @@ __global__ void __launch_bounds__(NT) router_topk_kernel(
   const int t = threadIdx.x;
   const int te = t % TGE, tm = t / TGE;
   const int n0 = blockIdx.x * BT;
+  grid_dep_wait();
+  grid_dep_launch();
 
   float acc_s[TM][TE], acc_c[TM][TE];
 #pragma unroll
@@ -203,9 +205,8 @@ moe_status_t launch(const void* xn, int N, int D, const float* w, const float* b
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return MOE_ERR_CUDA;
   const int grid = (N + BT - 1) / BT;
-  kern<<<grid, NT, smem, s>>>(static_cast<const XT*>(xn), w, bias, N, D, E, k, score_fn, logits,
-                              idx, gate, tie);
-  return launch_status();
+  return launch_kernel(kern, dim3(grid), dim3(NT), smem, s, static_cast<const XT*>(xn), w, bias, N, D, E, k,
+                       score_fn, logits, idx, gate, tie);
 }
 
 template <typename XT>
