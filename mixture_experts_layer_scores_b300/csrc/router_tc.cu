@@ -11,15 +11,15 @@
 // sum_d x_d * (hi_d + mid_d + lo_d) with fp32 accumulation.  The tensor core's own
 // accumulation over a long reduction is not correctly rounded (measured on B300: 7e-6 to
 // 2e-5 rms logit error when one accumulator spans all of D), so:
-//   * the hi plane is summed per 64-element slice in a fresh TMEM accumulator and the
-//     epilogue warps add the slice partials with two-sum compensation in registers
-//     (measured 8e-8 rms, about the fp32 rounding of the result);
-//   * the mid and lo planes, stacked as one N = 2*NT operand, accumulate across the whole
-//     reduction in a second accumulator: their error is scaled down by 2^-8.
-// Stacking mid and lo makes 8 MMAs per slice instead of 12 (an M=128 MMA costs 48, 64 and
-// 128 SM cycles at N = 64, 128 and 256, measured).  The hand-off per slice is one mbarrier arrival per
-// epilogue warp and a plain add per column, folded into the compensated total every 8
-// slices.  Short token counts are split along D (split-K) so that about
+//   * every 64-element slice of the reduction is summed in a fresh TMEM accumulator and
+//     the epilogue warps add the slice partials in registers, with two-sum compensation
+//     (measured 8e-8 rms for the hi plane alone, about the fp32 rounding of the result).
+// The three planes sit one after another in shared memory, so one MMA with N = 3*NT
+// covers all of them: 4 MMAs per slice.  The kernel is bound by issuing MMAs (one thread
+// issues them, at a cost per instruction well above the execution time of a narrow MMA),
+// which is why the planes share an instruction.  The hand-off per slice is one mbarrier
+// arrival per epilogue warp and a plain add per column (hi + (mid + lo)), folded into the
+// compensated total every 8 slices.  Short token counts are split along D (split-K) so that about
 // 128 CTAs stream the activations; the top-k kernel adds the split partials in order.
 //
 // Kernels: split (w -> 3 bf16 planes), router GEMM (tcgen05, logits [N, E] fp32), and a
@@ -62,37 +62,24 @@ struct Cfg {
   static constexpr int B_BYTES = NT * BK * 2;  // one split plane
   static constexpr int STAGE_BYTES = A_BYTES + 3 * B_BYTES;
   static constexpr int STAGES = NT >= 64 ? 4 : 6;
-  static constexpr int NBUF = NT >= 64 ? 4 : 8;        // hi-plane slice accumulators
-  static constexpr int L_COL = NBUF * NT;              // mid+lo accumulator (2*NT columns)
-  static constexpr int TMEM_COLS = (NBUF + 2) * NT <= 256 ? ((NBUF + 2) * NT <= 128 ? 128 : 256) : 512;
+  static constexpr int ACC = 3 * NT;                  // one slice accumulator: [hi | mid | lo]
+  static constexpr int NBUF = 512 / ACC < 8 ? 512 / ACC : 8;  // slice accumulators in TMEM
+  static constexpr int TMEM_COLS = NBUF * ACC <= 256 ? (NBUF * ACC <= 128 ? 128 : 256) : 512;
   static constexpr int EPI = NT >= 32 ? 8 : 4;         // epilogue warps
   static constexpr int W = NT / (EPI / 4);             // columns per epilogue thread
   static constexpr int THREADS = 96 + 32 * EPI;       // + warp 2 + EPI: activation copies
   static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES + 512;
 };
 
-// Load W consecutive fp32 TMEM columns (W = 16 or 32) of this warp's lane quarter.
-template <int W>
-__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&v)[W]) {
-  if constexpr (W == 16) {
-    uint32_t r[16];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-          "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-    tmem_ld_wait();
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-  } else {
-    uint32_t r[32];
-    tmem_ld32(taddr, r);
-    tmem_ld_wait();
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-  }
+// Start loading 16 consecutive fp32 TMEM columns of this warp's lane quarter (complete
+// with tmem_ld_wait()).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
 }
 
 // grid (ceil(N/128), ceil(E/NT)); block = TMA warp, MMA warp, EPI epilogue warps.
@@ -102,15 +89,14 @@ router_gemm_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_const
                    int N, int D, int E, int kb_per_split,
                    float* __restrict__ logits, float* __restrict__ partials, int* __restrict__ status) {
   using C = Cfg<NT>;
-  constexpr uint32_t IDESC_H = idesc_bf16(BM, NT);
-  constexpr uint32_t IDESC_L = idesc_bf16(BM, 2 * NT);
+  constexpr uint32_t IDESC = idesc_bf16(BM, 3 * NT);
   constexpr int STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   constexpr int NBUF = C::NBUF;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES);
-  // bars: full[STAGES], empty[STAGES], tfull[NBUF], tempty[NBUF], done, lfull
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 2 * NBUF + 2);
+  // bars: full[STAGES], empty[STAGES], tfull[NBUF], tempty[NBUF], done
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 2 * NBUF + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
@@ -122,7 +108,6 @@ router_gemm_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_const
   auto tfull_bar = [&](int a) { return smem_u32(bars + 2 * STAGES + a); };
   auto tempty_bar = [&](int a) { return smem_u32(bars + 2 * STAGES + NBUF + a); };
   const uint32_t done_bar = smem_u32(bars + 2 * STAGES + 2 * NBUF);
-  const uint32_t lfull_bar = smem_u32(bars + 2 * STAGES + 2 * NBUF + 1);
 
   if (t == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -134,7 +119,6 @@ router_gemm_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_const
       mbar_init(tempty_bar(a), C::EPI);  // one arrival per epilogue warp
     }
     mbar_init(done_bar, 1);
-    mbar_init(lfull_bar, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -187,16 +171,13 @@ router_gemm_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_const
 #pragma unroll
         for (int k = 0; k < BK / UK; ++k) {
           const uint64_t ad = sw128_desc(a_base + k * UK * 2);
-          tc_mma(tmem_base + (uint32_t)(acc * NT), ad, sw128_desc(b_base + k * UK * 2), IDESC_H, k ? 1u : 0u);
-          tc_mma(tmem_base + (uint32_t)C::L_COL, ad, sw128_desc(b_base + C::B_BYTES + k * UK * 2), IDESC_L,
-                 (kb > kb0 || k) ? 1u : 0u);
+          tc_mma(tmem_base + (uint32_t)(acc * C::ACC), ad, sw128_desc(b_base + k * UK * 2), IDESC, k ? 1u : 0u);
         }
         tc_commit(empty_bar(stage));
         tc_commit(tfull_bar(acc));
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         if (++acc == NBUF) { acc = 0; acc_phase ^= 1u; }
       }
-      tc_commit(lfull_bar);
       tc_commit(done_bar);
       mbar_wait(done_bar, 0, abort_flag, status, false);
     }
@@ -232,39 +213,26 @@ router_gemm_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_const
       ok = __shfl_sync(0xffffffffu, got, 0) != 0;
       if (!ok) break;
       tc_fence_after();
-      float p[W];
-      tmem_ld_cols<W>(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * NT + cb), p);
+      // this slice's partials of the three planes, 16 columns at a time: hi + (mid + lo)
+      const uint32_t ab = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * C::ACC + cb);
+#pragma unroll
+      for (int h = 0; h < W; h += 16) {
+        uint32_t rh[16], rm[16], rl[16];
+        tmem_ld16(ab + (uint32_t)h, rh);
+        tmem_ld16(ab + (uint32_t)(NT + h), rm);
+        tmem_ld16(ab + (uint32_t)(2 * NT + h), rl);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          loc[h + j] += __uint_as_float(rh[j]) + (__uint_as_float(rm[j]) + __uint_as_float(rl[j]));
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty_bar(acc));
-#pragma unroll
-      for (int j = 0; j < W; ++j) loc[j] += p[j];
       if (((kb - kb0) & 7) == 7) fold();
       if (++acc == NBUF) { acc = 0; acc_phase ^= 1u; }
     }
     fold();
-    if (ok) {
-      int got = 1;
-      if (lane == 0) got = mbar_wait(lfull_bar, 0, abort_flag, status, true) ? 1 : 0;
-      __syncwarp();
-      ok = __shfl_sync(0xffffffffu, got, 0) != 0;
-    }
-    if (ok) {  // mid and lo plane sums of this thread's columns
-      tc_fence_after();
-      const uint32_t lb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)C::L_COL;
-      float pm[W], pl[W];
-      tmem_ld_cols<W>(lb + (uint32_t)cb, pm);
-      tmem_ld_cols<W>(lb + (uint32_t)(NT + cb), pl);
-#pragma unroll
-      for (int j = 0; j < W; ++j) {
-        const float b = pm[j] + pl[j];
-        const float a = s[j];
-        const float tt = a + b;
-        const float bp = tt - a;
-        c[j] += (a - (tt - bp)) + (b - bp);
-        s[j] = tt;
-      }
-    }
     if (ok && row < N) {
       const int e1 = e0 + cb;
       float* dst = (blockIdx.z == 0 ? logits : partials + (size_t)(blockIdx.z - 1) * N * E) + (size_t)row * E + e1;
