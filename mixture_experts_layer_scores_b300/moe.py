@@ -96,6 +96,20 @@ def _chk(name, st):
         raise MoEError(name, st)
 
 
+def _need(name, t, dtype=None, shape=None, device=None):
+    """Check one tensor argument before its pointer reaches the library.  The kernels trust
+    the sizes passed beside the pointers, so a wrong dtype, shape or device here would make
+    them read or write past a buffer; None (an optional argument left out) passes."""
+    if t is None:
+        return
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name}: on {t.device}, expected {device}")
+
+
 def _cuda(*ts):
     for t in ts:
         if t is not None and (not t.is_cuda or not t.is_contiguous()):
@@ -117,6 +131,12 @@ def moe_router_topk(xn, w_router, bias, k, score_fn="softmax", logits_out=None, 
     N, D = xn.shape
     E = w_router.shape[0]
     dev = xn.device
+    _need("w_router", w_router, torch.float32, (E, D), dev)
+    _need("bias", bias, torch.float32, (E,), dev)
+    _need("logits_out", logits_out, torch.float32, (N, E), dev)
+    _need("topk_idx", topk_idx, torch.int32, (N, k), dev)
+    _need("topk_gate", topk_gate, torch.float32, (N, k), dev)
+    _need("near_tie", near_tie, torch.uint8, (N,), dev)
     if logits_out is None and want_logits:
         logits_out = torch.empty(N, E, dtype=torch.float32, device=dev)
     if topk_idx is None:
@@ -136,6 +156,8 @@ def moe_router_split(w_router, w_split=None, stream=None):
     """fp32 [E, D] router weight -> bf16 [3, E, D] planes with hi + mid + lo == w exactly."""
     L = load()
     E, D = w_router.shape
+    _need("w_router", w_router, torch.float32)
+    _need("w_split", w_split, torch.bfloat16, (3, E, D), w_router.device)
     if w_split is None:
         w_split = torch.empty(3, E, D, dtype=torch.bfloat16, device=w_router.device)
     _cuda(w_router, w_split)
@@ -155,6 +177,14 @@ def moe_router_topk_split(xn, w_split, bias, k, score_fn="softmax", logits_out=N
     N, D = xn.shape
     E = w_split.shape[1]
     dev = xn.device
+    _need("xn", xn, torch.bfloat16)
+    _need("w_split", w_split, torch.bfloat16, (3, E, D), dev)
+    _need("bias", bias, torch.float32, (E,), dev)
+    _need("logits_out", logits_out, torch.float32, (N, E), dev)
+    _need("topk_idx", topk_idx, torch.int32, (N, k), dev)
+    _need("topk_gate", topk_gate, torch.float32, (N, k), dev)
+    _need("near_tie", near_tie, torch.uint8, (N,), dev)
+    _need("workspace", workspace, device=dev)
     if logits_out is None:
         logits_out = torch.empty(N, E, dtype=torch.float32, device=dev)
     if topk_idx is None:
@@ -191,6 +221,15 @@ def moe_permute(xn, topk_idx, E, counts=None, offsets=None, row_map=None, perm_t
     N, k = topk_idx.shape
     dev = topk_idx.device
     D = xn.shape[1] if xn is not None else 64
+    _need("topk_idx", topk_idx, torch.int32)
+    if xn is not None:
+        _need("xn", xn, shape=(N, D), device=dev)
+    _need("counts", counts, torch.int32, (E,), dev)
+    _need("offsets", offsets, torch.int32, (E + 1,), dev)
+    _need("row_map", row_map, torch.int32, (N, k), dev)
+    _need("perm_token", perm_token, torch.int32, (N * k,), dev)
+    _need("x_perm", x_perm, None if xn is None else xn.dtype, (N * k, D), dev)
+    _need("workspace", workspace, device=dev)
     if counts is None:
         counts = torch.empty(E, dtype=torch.int32, device=dev)
     if offsets is None:
@@ -227,6 +266,14 @@ def moe_permute_noalloc(xn, topk_idx, E, counts, offsets, row_map, perm_token, x
     L = load()
     N, k = topk_idx.shape
     D = xn.shape[1]
+    dev = topk_idx.device
+    _need("topk_idx", topk_idx, torch.int32)
+    _need("xn", xn, shape=(N, D), device=dev)
+    _need("counts", counts, torch.int32, (E,), dev)
+    _need("offsets", offsets, torch.int32, (E + 1,), dev)
+    _need("row_map", row_map, torch.int32, (N, k), dev)
+    _need("perm_token", perm_token, torch.int32, (N * k,), dev)
+    _need("x_perm", x_perm, xn.dtype, (N * k, D), dev)
     _cuda(xn, topk_idx, counts, offsets, row_map, perm_token, x_perm)
     _chk("moe_permute_noalloc", L.moe_permute_noalloc(
         _p(xn), _dt(xn), N, D, _p(topk_idx), k, E, _p(counts), _p(offsets), _p(row_map),
@@ -241,6 +288,13 @@ def moe_grouped_swiglu(x_perm, offsets, w_gate, w_up, w_down, h_workspace=None, 
     L = load()
     M, D = x_perm.shape
     G, F, _ = w_gate.shape
+    dt, dev = x_perm.dtype, x_perm.device
+    _need("offsets", offsets, torch.int32, (G + 1,), dev)
+    _need("w_gate", w_gate, dt, (G, F, D), dev)
+    _need("w_up", w_up, dt, (G, F, D), dev)
+    _need("w_down", w_down, dt, (G, D, F), dev)
+    _need("h_workspace", h_workspace, dt, (M, F), dev)
+    _need("y_perm", y_perm, dt, (M, D), dev)
     if h_workspace is None:
         h_workspace = torch.empty(M, F, dtype=x_perm.dtype, device=x_perm.device)
     if y_perm is None:
@@ -259,6 +313,15 @@ def moe_grouped_swiglu_gather(xn, perm_token, offsets, w_gate, w_up, w_down, h_w
     M = perm_token.shape[0]
     N, D = xn.shape
     G, F, _ = w_gate.shape
+    dt, dev = xn.dtype, xn.device
+    _need("xn", xn, torch.bfloat16)
+    _need("perm_token", perm_token, torch.int32, (M,), dev)
+    _need("offsets", offsets, torch.int32, (G + 1,), dev)
+    _need("w_gate", w_gate, dt, (G, F, D), dev)
+    _need("w_up", w_up, dt, (G, F, D), dev)
+    _need("w_down", w_down, dt, (G, D, F), dev)
+    _need("h_workspace", h_workspace, dt, (M, F), dev)
+    _need("y_perm", y_perm, dt, (M, D), dev)
     if h_workspace is None:
         h_workspace = torch.empty(M, F, dtype=xn.dtype, device=xn.device)
     if y_perm is None:
@@ -276,6 +339,12 @@ def moe_unpermute_combine(y_perm, row_map, topk_gate, shared_y=None, residual=No
     L = load()
     N, k = row_map.shape
     D = y_perm.shape[1]
+    dt, dev = y_perm.dtype, y_perm.device
+    _need("row_map", row_map, torch.int32, device=dev)
+    _need("topk_gate", topk_gate, torch.float32, (N, k), dev)
+    _need("shared_y", shared_y, dt, (N, D), dev)
+    _need("residual", residual, dt, (N, D), dev)
+    _need("out", out, dt, (N, D), dev)
     if out is None:
         out = torch.empty(N, D, dtype=y_perm.dtype, device=y_perm.device)
     _cuda(y_perm, row_map, topk_gate, shared_y, residual, out)
@@ -289,6 +358,9 @@ def moe_bias_update(counts, bias, total_assignments, gamma, max_over_mean=None, 
     """bias += gamma * sign(total/E - counts), in place.  Returns max_over_mean (device fp32[1])."""
     L = load()
     E = counts.shape[0]
+    _need("counts", counts, torch.int32)
+    _need("bias", bias, torch.float32, (E,), counts.device)
+    _need("max_over_mean", max_over_mean, torch.float32, (1,), counts.device)
     if max_over_mean is None:
         max_over_mean = torch.empty(1, dtype=torch.float32, device=counts.device)
     _cuda(counts, bias, max_over_mean)
