@@ -31,6 +31,10 @@
  *    moe_last_device_status), so a sequence of calls can be captured in a CUDA graph
  *    once each entry point has run once on the device.
  *  - Results are deterministic: the same inputs give the same bits, run to run.
+ *  - Kernels are launched with programmatic dependent launch: each may start while the
+ *    kernel before it on the stream drains, and waits for that kernel to complete before
+ *    it touches global memory, so stream order means what it always does.  MOE_PDL=0 in
+ *    the environment (read once per process) launches them plainly; results are the same.
  */
 #ifndef MOE_B300_H
 #define MOE_B300_H
