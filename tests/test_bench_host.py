@@ -1,0 +1,72 @@
+"""Host-side logic of bench.py, no GPU: the algorithmic work the roofline divides by, the
+traffic record's tie to the kernel sources, and the reference arm's JSON line."""
+import json
+import os
+import shutil
+import subprocess
+import sys
+
+import bench
+from mixture_experts_layer_scores_b300 import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+C = synth.CONFIGS
+
+
+def test_algorithmic_work_matches_closed_forms():
+    # handbook layer: R = N k = 65536 rows of D = 2048, F = 1024, bf16
+    a = bench.algorithmic(C["handbook"])
+    assert a["gemm_flops"] == 6 * 65536 * 2048 * 1024                    # 824.6 GFLOP
+    assert a["combine_bytes"] == 65536 * 2048 * 2 + 8 * 65536 + 2 * 8192 * 2048 * 2  # 336.1 MB
+    assert a["permute_bytes"] == 12 * 65536                                # gathering: ids only
+    copy = bench.algorithmic(C["handbook"], copy_rows=True)
+    assert copy["permute_bytes"] == 8192 * 2048 * 2 + 65536 * 2048 * 2 + 12 * 65536  # 302.8 MB
+    assert a["router_flops"] == 2 * 8192 * 2048 * 64
+    # DeepSeek-V3 shape: the shared expert's row joins the combine
+    d = bench.algorithmic(C["deepseek_v3"])
+    assert d["combine_bytes"] == 32768 * 7168 * 2 + 8 * 32768 + 3 * 4096 * 7168 * 2  # 646.2 MB
+    assert d["shared_flops"] == 6 * 4096 * 7168 * 2048
+
+
+def _tree(tmp, alter=None):
+    srcs = ["mixture_experts_layer_scores_b300/csrc/grouped_swiglu.cu",
+            "mixture_experts_layer_scores_b300/csrc/tc_common.cuh",
+            "mixture_experts_layer_scores_b300/csrc/moe_internal.cuh"]
+    for rel in srcs + ["profiles/grouped_gemm_handbook_traffic.txt",
+                       "profiles/grouped_gemm_handbook_gather_traffic.txt"]:
+        dst = os.path.join(tmp, rel)
+        os.makedirs(os.path.dirname(dst), exist_ok=True)
+        shutil.copy(os.path.join(ROOT, rel), dst)
+    if alter:
+        with open(os.path.join(tmp, alter), "a") as f:
+            f.write("\n// changed\n")
+
+
+def test_traffic_record_holds_only_for_the_recorded_sources(tmp_path, monkeypatch):
+    same, changed = tmp_path / "same", tmp_path / "changed"
+    _tree(str(same))
+    _tree(str(changed), alter="mixture_experts_layer_scores_b300/csrc/grouped_swiglu.cu")
+    monkeypatch.setattr(bench, "ROOT", str(same))
+    gather, copy = bench.recorded_traffic(C["handbook"], True), bench.recorded_traffic(C["handbook"], False)
+    assert gather and copy and gather != copy
+    assert bench.recorded_traffic(C["mixtral"], False) is None  # no record for that workload
+    monkeypatch.setattr(bench, "ROOT", str(changed))
+    assert bench.recorded_traffic(C["handbook"], True) is None
+    assert bench.recorded_traffic(C["handbook"], False) is None
+
+
+def test_reference_arm_prints_one_complete_line():
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                          "--warmup", "1", "--config", "tiny"], capture_output=True, text=True, timeout=600,
+                         check=True, cwd=ROOT).stdout
+    lines = [json.loads(l) for l in out.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = lines[0]
+    assert d["impl"] == "reference" and d["unit"] == "tokens/s" and d["value"] > 0
+    for key in ("metric", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
+                "vs_baseline", "dtype", "data", "config"):
+        assert key in d, key
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["cpu_baseline"]["value"] == d["value"] and d["cpu_baseline"]["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    assert "tiny" in d["config"]["workload"]
