@@ -28,7 +28,7 @@ Sources, cited by page title and section:
   dimensions table and section "1. 专家负载均衡的评测" (per-expert routed-token
   histogram).
 
-Readings where the pages leave a step open (each listed again in the design doc):
+Readings where the pages leave a step open:
 
 * Sigmoid router: selection on sigma(logit) + bias, gates sigma_i / sum over the
   chosen sigma_j (unbiased).  No routed scaling factor, no group limit.
