@@ -51,7 +51,7 @@ typedef struct CUstream_st* moe_stream_t; /* a cudaStream_t; NULL = legacy defau
 typedef enum moe_status {
   MOE_OK = 0,
   MOE_ERR_INVALID_ARG = -1, /* null/unaligned pointer, size out of range, bad id */
-  MOE_ERR_UNSUPPORTED = -2, /* shape or dtype this build does not run */
+  MOE_ERR_UNSUPPORTED = -2, /* shape or dtype the library does not run */
   MOE_ERR_CUDA = -3,        /* a CUDA runtime call or kernel launch failed */
   MOE_ERR_TIMEOUT = -4,     /* a device-side wait gave up (status word) */
   MOE_ERR_NAN_INPUT = -5    /* reserved for input screening */
