@@ -70,3 +70,13 @@ def test_reference_arm_prints_one_complete_line():
     assert d["cpu_baseline"]["value"] == d["value"] and d["cpu_baseline"]["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
     assert "tiny" in d["config"]["workload"]
+
+
+def test_clock_records_that_invalidate_a_number():
+    ok = {"sm_mhz": 1432.0, "sm_max_mhz": 2032.0, "reasons": ["sw_power_cap"]}
+    assert bench.clock_problem(ok) is None
+    assert bench.clock_problem({"sm_mhz": 2000.0, "sm_max_mhz": 2032.0, "reasons": []}) is None
+    assert "hw_thermal_slowdown" in bench.clock_problem(dict(ok, reasons=["hw_thermal_slowdown", "sw_power_cap"]))
+    assert "sw_thermal_slowdown" in bench.clock_problem(dict(ok, reasons=["sw_thermal_slowdown"]))
+    assert "no reason" in bench.clock_problem({"sm_mhz": 900.0, "sm_max_mhz": 2032.0, "reasons": []})
+    assert bench.clock_problem({"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}) is None
