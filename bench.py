@@ -3,8 +3,11 @@
 
 One step = one pass of the whole layer over one batch: router GEMM + biased top-k +
 gates, histogram + scan + permute, grouped SwiGLU GEMMs (+ shared expert), gated
-combine, and the +-gamma bias step.  Default workload: the handbook teaching-model
-layer (N=8192 tokens, d_model=2048, 64 experts of d_ff=1024, top-8, softmax gates).
+combine, and the +-gamma bias step.  Headline workload: the DeepSeek-V3-shaped layer
+(N=4096 tokens, d_model=7168, 256 routed experts of d_ff=2048 plus one shared expert,
+top-8, sigmoid scores normalised over the chosen 8), the largest single-GPU layer of the
+five; the line's `per_config` object measures the other four (handbook, Mixtral-shaped,
+Zipf-skewed at k=8 and k=4, all-fp32 tiny) the same way.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl reference]
 
@@ -16,8 +19,8 @@ from __future__ import annotations
 
 import argparse
 import json
-import math
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -34,6 +37,14 @@ from mixture_experts_layer_scores_b300 import moe, synth  # noqa: E402
 
 METRIC = "MoE-layer fwd tokens/s; grouped-GEMM TFLOP/s & permute GB/s vs B300 peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+DEFAULT_CONFIG = "deepseek_v3"
+# (label, configuration, experts per token): the workloads of the line's per_config object
+WORKLOADS = [("deepseek_v3", "deepseek_v3", 8), ("handbook", "handbook", 8), ("mixtral", "mixtral", 2),
+             ("skewed_k8", "skewed", 8), ("skewed_k4", "skewed", 4), ("tiny", "tiny", 2)]
+# fp32 FMA peak of the all-fp32 layer's CUDA-core kernels: 148 SMs x 128 lanes x 2 flops x 2.032 GHz
+F32_ALU_TFLOPS = 148 * 128 * 2 * 2.032e9 / 1e12
+# tokens of the workload the oracle runs per timed sample (about a second of host work each)
+ORACLE_SAMPLE_TOKENS = {"tiny": 512, "handbook": 512, "mixtral": 16, "deepseek_v3": 6, "skewed": 512}
 
 
 def peaks():
@@ -68,11 +79,25 @@ def recorded_traffic(cfg, gather):
     return int(kv["dram_bytes_per_call"])
 
 
-def workload_name(cfg):
-    s = f"{cfg.name}: N={cfg.N} D={cfg.D} E={cfg.E} F={cfg.F} k={cfg.k} {cfg.score_fn}"
+def workload_name(cfg, k=None):
+    k = cfg.k if k is None else k
+    s = f"{cfg.name}: N={cfg.N} D={cfg.D} E={cfg.E} F={cfg.F} k={k} {cfg.score_fn}"
     if cfg.shared:
         s += f" +{cfg.shared} shared(F={cfg.F_shared})"
+    if cfg.zipf_s:
+        s += f" zipf({cfg.zipf_s})"
+    if cfg.dtype != "bf16":
+        s += f" all-{cfg.dtype}"
     return s
+
+
+def config_dict(cfg, k, world):
+    """The `config` object of both arms' lines: the workload only (the same dict in both)."""
+    wbytes = 3 * cfg.E * cfg.D * cfg.F * (2 if cfg.dtype == "bf16" else 4)
+    return {"workload": workload_name(cfg, k), "tokens_per_gpu": cfg.N,
+            "l2": "no flush: every step streams %.0f MB of expert weights (L2 126 MB)" % (wbytes / 1e6)
+                  if wbytes > 126e6 else "no flush: the whole layer fits in L2 (%.1f MB of weights)" % (wbytes / 1e6),
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
 
 
 def algorithmic(cfg, k=None, copy_rows=False):
@@ -87,9 +112,11 @@ def algorithmic(cfg, k=None, copy_rows=False):
         router_flops=2.0 * N * D * E,
         router_bytes=N * D * b + E * D * 4 + N * E * 4 + N * k * 8 + N,
         permute_bytes=(N * D * b + R * D * b if copy_rows else 0) + 12.0 * R,
+        permute_copy_bytes=N * D * b + R * D * b + 12.0 * R,
         gemm_flops=6.0 * R * D * F,
         gemm_bytes=3.0 * E * D * F * b + R * D * b + 2.0 * R * F * b + R * D * b,
         shared_flops=6.0 * N * D * Fs * S,
+        shared_bytes=(3.0 * D * Fs * b + N * D * b + 2.0 * N * Fs * b + N * D * b) * S,
         combine_bytes=R * D * b + 8.0 * R + (2 + S) * N * D * b,
     )
 
@@ -166,26 +193,35 @@ def clock_problem(summary):
     return None
 
 
+def cpu_model():
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.processor() or "unknown"
+
+
 # ------------------------------------------------------------------------------------------
 # CUDA arm
 # ------------------------------------------------------------------------------------------
 
-class Step:
-    """One layer forward + bias step with CUDA events between the stages."""
+class Workload:
+    """One layer (weights, tokens, reusable buffers) and its step: forward + bias step."""
 
     STAGES = ("router", "permute", "grouped_swiglu", "shared", "combine", "bias")
 
-    def __init__(self, cfg, dev, rank, world, gather=None):
-        self.cfg, self.dev, self.world = cfg, dev, world
-        seed_tok = cfg.seed + 1000 * rank
-        xn, h = synth.make_tokens(cfg, dev, seed=seed_tok)
-        self.xn, self.h = xn, h
+    def __init__(self, cfg, k, dev, rank=0, world=1, gather=None):
+        self.cfg, self.k, self.dev, self.world = cfg, k, dev, world
+        self.xn, self.h = synth.make_tokens(cfg, dev, seed=cfg.seed + 1000 * rank)
         w_r, b = synth.make_router(cfg, dev)
         wg, wu, wd = synth.make_experts(cfg, dev)
         sh = synth.make_shared(cfg, dev)
-        self.layer = moe.MoELayer(moe.LayerWeights(w_r, b, wg, wu, wd, sh), cfg.N, cfg.k,
-                                  cfg.score_fn, cfg.gamma, gather=gather)
-        self.ev = None
+        dt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
+        self.layer = moe.MoELayer(moe.LayerWeights(w_r, b, wg, wu, wd, sh), cfg.N, k, cfg.score_fn,
+                                  cfg.gamma, dtype=dt, gather=gather)
 
     def run(self, xn=None, h=None, events=None, out=None):
         L = self.layer
@@ -213,65 +249,115 @@ class Step:
         return self.layer.kernels_per_forward
 
 
-def time_device(step, steps, warmup, world):
-    """The headline: K forwards + bias steps back to back, with events at the ends only.  On
-    one GPU each step replays a CUDA graph of the layer (MoELayer.capture); with replicas the
-    steps launch eagerly, since the counts all-reduce sits between the forward and the bias
-    step.  Then K more eager steps with events between the stages give the per-stage times
-    (the grouped GEMM's among them, for the roofline).  Returns (ms for the K headline
-    steps, stage µs, launch mode)."""
-    for _ in range(warmup):
-        step.run()
-    fwd, mode = step.run, "eager"
-    if world == 1:
-        fwd, mode = step.layer.capture(step.xn, step.h), "cuda graph of the layer (MoELayer.capture)"
-        for _ in range(warmup):
-            fwd()
-    torch.cuda.synchronize()
+def _timed(fn, steps):
+    """Device ms for `steps` calls of fn on the current stream (events at the ends only)."""
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    if world > 1:
-        torch.distributed.barrier()
     torch.cuda.synchronize()
     t0.record()
     for _ in range(steps):
-        fwd()
+        fn()
     t1.record()
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1)
+
+
+def time_device(wl, steps, warmup, world):
+    """The headline: K forwards + bias steps back to back, events at the ends only.  On one
+    GPU each step replays a CUDA graph of the layer (MoELayer.capture); with replicas the
+    steps launch eagerly, since the counts all-reduce sits between the forward and the bias
+    step.  Returns (ms for the K steps, launch mode)."""
+    for _ in range(warmup):
+        wl.run()
+    fwd, mode = wl.run, "eager"
+    if world == 1:
+        fwd, mode = wl.layer.capture(wl.xn, wl.h), "cuda graph of the layer (MoELayer.capture)"
+        for _ in range(warmup):
+            fwd()
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    total_ms = t0.elapsed_time(t1)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(steps)]
-    for i in range(steps):
-        step.run(events=evs[i])
+    ms = _timed(fwd, steps)
+    if world > 1:
+        torch.distributed.barrier()
+    return ms, mode
+
+
+def stage_times(wl, steps, world):
+    """Per-stage device µs over `steps` steps run back to back, as in the headline, with
+    timing events between the stages.  On one GPU every step is the replay of its own CUDA
+    graph of the layer (events captured as graph nodes, one event set per graph, so the
+    replays need no synchronisation between them).  The event nodes cut the programmatic
+    overlap of the kernels on both sides of each, so the stage sum runs a little above
+    the headline step.  With replicas: eager steps."""
+    evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(7)] for _ in range(steps)]
+    if world == 1:
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        graphs = []
+        for i in range(steps):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                wl.run(events=evs[i])
+            graphs.append(g)
+        torch.cuda.current_stream().wait_stream(s)
+        for g in graphs[:3]:  # warm
+            g.replay()
+        steps_fn = [g.replay for g in graphs]
+        how = "back-to-back replays of CUDA graphs of the step with event nodes between the stages"
+    else:
+        steps_fn = [(lambda e=e: wl.run(events=e)) for e in evs]
+        how = "eager steps with events between the stages"
     torch.cuda.synchronize()
-    stage_us = {}
-    for j, name in enumerate(Step.STAGES):
-        stage_us[name] = 1e3 * statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs)
-    return total_ms, stage_us, mode
+    for fn in steps_fn:
+        fn()
+    torch.cuda.synchronize()
+    acc = {n: [e[j].elapsed_time(e[j + 1]) for e in evs] for j, n in enumerate(Workload.STAGES)}
+    return {n: 1e3 * statistics.mean(v) for n, v in acc.items()}, how
 
 
-def time_e2e(step, steps, warmup, world):
+def time_permute_copy(wl, steps):
+    """The permute with the row copy (x_perm written) on the layer's routing, graph replays:
+    the HBM-bound form of the step, measured also where the layer's GEMM gathers instead."""
+    L, cfg = wl.layer, wl.cfg
+    x_perm = torch.empty(cfg.N * wl.k, cfg.D, dtype=wl.xn.dtype, device=wl.xn.device)
+    cnt, off = torch.empty_like(L.counts), torch.empty_like(L.offsets)
+    rm, pt = torch.empty_like(L.row_map), torch.empty_like(L.perm_token)
+    fn = lambda: moe.moe_permute(wl.xn, L.idx, L.E, cnt, off, rm, pt, x_perm, L.workspace)
+    fn()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        fn()
+    torch.cuda.current_stream().wait_stream(s)
+    g.replay()
+    us = 1e3 * _timed(g.replay, steps) / steps
+    del x_perm
+    return us
+
+
+def time_e2e(wl, steps, warmup, world):
     """The layer fed from and drained to pinned host memory every step, the way a serving
     loop runs it: two sets of device buffers, host-to-device copies of step i+1 and the
     device-to-host copy of step i-1 on their own streams while step i computes."""
-    cfg = step.cfg
-    hx = step.xn.cpu().pin_memory()
-    hh = step.h.cpu().pin_memory()
+    cfg = wl.cfg
+    hx = wl.xn.cpu().pin_memory()
+    hh = wl.h.cpu().pin_memory()
     nb = 2
-    hout = [torch.empty(cfg.N, cfg.D, dtype=step.xn.dtype).pin_memory() for _ in range(nb)]
-    dx = [torch.empty_like(step.xn) for _ in range(nb)]
-    dh = [torch.empty_like(step.h) for _ in range(nb)]
-    dout = [torch.empty(cfg.N, cfg.D, dtype=step.xn.dtype, device=step.xn.device) for _ in range(nb)]
+    hout = [torch.empty(cfg.N, cfg.D, dtype=wl.xn.dtype).pin_memory() for _ in range(nb)]
+    dx = [torch.empty_like(wl.xn) for _ in range(nb)]
+    dh = [torch.empty_like(wl.h) for _ in range(nb)]
+    dout = [torch.empty(cfg.N, cfg.D, dtype=wl.xn.dtype, device=wl.xn.device) for _ in range(nb)]
     comp = torch.cuda.current_stream()
     for b in range(nb):
-        dx[b].copy_(step.xn)
-        dh[b].copy_(step.h)
+        dx[b].copy_(wl.xn)
+        dh[b].copy_(wl.h)
     if world == 1:  # one graph per buffer set, as in the device-timed leg
-        graphs = [step.layer.capture(dx[b], dh[b], out=dout[b]) for b in range(nb)]
+        graphs = [wl.layer.capture(dx[b], dh[b], out=dout[b]) for b in range(nb)]
         fwd = lambda b: graphs[b]()
     else:
-        fwd = lambda b: step.run(dx[b], dh[b], out=dout[b])
+        fwd = lambda b: wl.run(dx[b], dh[b], out=dout[b])
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
     ev = lambda: [torch.cuda.Event() for _ in range(nb)]
     in_ready, used, out_ready, out_copied = ev(), ev(), ev(), ev()
@@ -317,44 +403,98 @@ def time_e2e(step, steps, warmup, world):
     return ms, 2 * cfg.N * cfg.D * b, cfg.N * cfg.D * b
 
 
-def fresh_layer(step, k):
-    """A layer on the step's weights and tokens with the initial bias and k experts per token."""
-    cfg, w = step.cfg, step.layer.w
-    b0 = synth.make_router(cfg, step.dev)[1]
+def fresh_layer(wl, k):
+    """A layer on the workload's weights with the initial bias and k experts per token."""
+    cfg, w = wl.cfg, wl.layer.w
+    b0 = synth.make_router(cfg, wl.dev)[1]
+    dt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
     return moe.MoELayer(moe.LayerWeights(w.w_router, b0, w.w_gate, w.w_up, w.w_down, w.shared), cfg.N, k,
-                        cfg.score_fn, cfg.gamma)
+                        cfg.score_fn, cfg.gamma, dtype=dt)
 
 
-def load_balance_trace(step, steps=50):
-    """max/mean expert load after each of `steps` forwards with the +-gamma bias step, from the
-    initial bias (untimed)."""
-    L = fresh_layer(step, step.cfg.k)
+def load_balance_trace(wl, steps=50):
+    """max/mean expert load of each of `steps` forwards, each on a fresh seeded batch
+    (seed * 1000 + t) and each followed by the +-gamma bias step, from the initial bias
+    (untimed)."""
+    L = fresh_layer(wl, wl.k)
     trace = []
-    for _ in range(steps):
-        L.forward(step.xn, step.h)
-        trace.append(round(float(L.mom.item()), 4))
-    return {"gamma": step.cfg.gamma, "steps": steps, "max_over_mean_per_step": trace}
-
-
-def time_fewer_experts(step, k, steps, warmup):
-    """The same weights served with k experts per token instead of cfg.k (gates renormalise
-    over the k chosen): tokens/s over `steps` timed forwards."""
-    cfg, xn, h = step.cfg, step.xn, step.h
-    L = fresh_layer(step, k)
-    for _ in range(warmup):
+    for t in range(steps):
+        xn, h = synth.make_tokens(wl.cfg, wl.dev, seed=wl.cfg.seed * 1000 + t)
         L.forward(xn, h)
-    fwd = L.capture(xn, h)  # replayed as in the headline leg
-    for _ in range(warmup):
-        fwd()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(steps):
-        fwd()
-    e1.record()
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / steps
-    return {"k": k, "tokens_per_s": cfg.N / (ms * 1e-3), "ms_per_step": ms}
+        trace.append(round(float(L.mom.item()), 4))
+    return {"gamma": wl.cfg.gamma, "steps": steps, "batches": "fresh seeded batch per step",
+            "max_over_mean_per_step": trace}
+
+
+def roofline_of(flops, bytes_, us, pk, long_run, dtype):
+    """The bound of a kernel from its algorithmic flops and bytes (whichever takes longer at
+    the measured peaks), and its achieved fraction of that bound."""
+    if dtype != "bf16":
+        ach = flops / (us * 1e-6) / 1e12
+        return {"bound": "alu", "achieved": ach, "peak": F32_ALU_TFLOPS, "unit": "TFLOP/s",
+                "frac": ach / F32_ALU_TFLOPS, "peak_kind": "fp32 FMA rate: 148 SMs x 128 lanes x 2.032 GHz"}
+    pt = pk["bf16_tflops_sustained"] if long_run else pk["bf16_tflops"]
+    t_tensor = flops / (pt * 1e12)
+    t_hbm = bytes_ / (pk["hbm_gbs"] * 1e9)
+    if t_tensor >= t_hbm:
+        ach = flops / (us * 1e-6) / 1e12
+        return {"bound": "tensor", "achieved": ach, "peak": pt, "unit": "TFLOP/s", "frac": ach / pt,
+                "peak_kind": "bf16 " + ("sustained" if long_run else "burst"),
+                "frac_of_burst": ach / pk["bf16_tflops"]}
+    ach = bytes_ / (us * 1e-6) / 1e9
+    return {"bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": ach / pk["hbm_gbs"],
+            "peak_kind": "HBM copy", "tensor_frac": flops / (us * 1e-6) / 1e12 / pt}
+
+
+def measure(wl, steps, warmup, world, pk, e2e_steps):
+    """Every number of one workload: headline graph replays, stage times, roofline, e2e."""
+    cfg, k, L = wl.cfg, wl.k, wl.layer
+    total_ms, mode = time_device(wl, steps, warmup, world)
+    total_ms = max_over_ranks(total_ms, world)
+    st = moe.last_device_status()
+    if st != 0:
+        raise SystemExit(f"device status {moe.STATUS.get(st, st)} after {cfg.name} k={k}")
+    stage_us, how = stage_times(wl, steps, world)
+    ms = total_ms / steps
+    alg = algorithmic(cfg, k, copy_rows=not L.gather)
+    long_run = total_ms >= 1000.0
+    gemm = roofline_of(alg["gemm_flops"], alg["gemm_bytes"], stage_us["grouped_swiglu"], pk, long_run, cfg.dtype)
+    gbs = lambda b, us: b / (us * 1e-6) / 1e9
+    hbm = pk["hbm_gbs"]
+    copy_us = time_permute_copy(wl, steps)
+    res = {
+        "workload": workload_name(cfg, k), "tokens_per_s": cfg.N * world / (ms * 1e-3), "ms_per_step": ms,
+        "steps": steps, "launch": mode, "gemm1_rows": "gathered from xn" if L.gather else "permuted copy x_perm",
+        "stage_us": {n: round(v, 2) for n, v in stage_us.items()},
+        "stage_sum_us": round(sum(stage_us.values()), 2), "stage_us_from": how,
+        "grouped_gemm": dict(gemm, kernel="moe_grouped_swiglu_gather" if L.gather else "moe_grouped_swiglu",
+                             launches="GEMM1+SwiGLU and GEMM2", us=round(stage_us["grouped_swiglu"], 2),
+                             tflops=alg["gemm_flops"] / (stage_us["grouped_swiglu"] * 1e-6) / 1e12,
+                             algorithmic_gflop=alg["gemm_flops"] / 1e9,
+                             algorithmic_gb=alg["gemm_bytes"] / 1e9),
+        "router": {"gbs": gbs(alg["router_bytes"], stage_us["router"]),
+                   "frac_hbm": gbs(alg["router_bytes"], stage_us["router"]) / hbm,
+                   "algorithmic_mb": alg["router_bytes"] / 1e6, "launches": 3 if L.tc_router else 1},
+        "permute": {"moves_rows": not L.gather, "us": round(stage_us["permute"], 2),
+                    "gbs": gbs(alg["permute_bytes"], stage_us["permute"]) if not L.gather else None,
+                    "frac_hbm": gbs(alg["permute_bytes"], stage_us["permute"]) / hbm if not L.gather else None,
+                    "index_only_mb": 12.0 * cfg.N * k / 1e6 if L.gather else None},
+        "permute_with_row_copy": {"us": round(copy_us, 2), "gbs": gbs(alg["permute_copy_bytes"], copy_us),
+                                  "frac_hbm": gbs(alg["permute_copy_bytes"], copy_us) / hbm,
+                                  "algorithmic_mb": alg["permute_copy_bytes"] / 1e6},
+        "combine": {"gbs": gbs(alg["combine_bytes"], stage_us["combine"]),
+                    "frac_hbm": gbs(alg["combine_bytes"], stage_us["combine"]) / hbm,
+                    "algorithmic_mb": alg["combine_bytes"] / 1e6},
+        "gpu_launches_per_step": wl.launches,
+    }
+    if cfg.shared:
+        res["shared_expert"] = roofline_of(alg["shared_flops"], alg["shared_bytes"], stage_us["shared"], pk,
+                                           long_run, cfg.dtype)
+    e2e_ms, bi, bo = time_e2e(wl, e2e_steps, warmup, world)
+    e2e_ms = max_over_ranks(e2e_ms, world)
+    res["e2e"] = {"value": cfg.N * world / (e2e_ms / e2e_steps * 1e-3), "unit": "tokens/s",
+                  "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
+    return res, total_ms
 
 
 def max_over_ranks(x, world):
@@ -369,22 +509,62 @@ def max_over_ranks(x, world):
 # CPU oracle (the reference arm and the cpu_baseline leg)
 # ------------------------------------------------------------------------------------------
 
-def oracle_sample(cfg, n_tok):
-    """Inputs for the first n_tok tokens of the workload, plus the full weights (CPU)."""
-    rows = np.arange(n_tok)
-    xn, h = synth.make_tokens(cfg, "cpu", rows=rows)
-    w_r, b = synth.make_router(cfg, "cpu")
-    wg, wu, wd = synth.make_experts(cfg, "cpu")
-    sh = synth.make_shared(cfg, "cpu")
-    f = lambda t: t.to(torch.float32).numpy()
-    return dict(xn=f(xn), h=f(h), w_r=w_r.numpy(), b=b.numpy(), wg=f(wg), wu=f(wu), wd=f(wd),
-                sh=None if sh is None else tuple(f(t) for t in sh))
+class OracleSample:
+    """The oracle on the first n tokens of a workload, timed.
 
+    The oracle's own functions run in its layer order: route, counts, scan, stable
+    permutation, every visited expert's SwiGLU on its rows, the shared expert, the combine,
+    the bias step.  Expert weights are regenerated once per expert (synth.make_expert: the
+    same bits as the GPU's) and widened to float64 outside the timed sections, one expert
+    at a time, so the largest layer (22.6 GB of bf16 weights) never sits in host memory.
+    """
 
-def run_oracle(cfg, s):
-    from oracle import moe_oracle
-    return moe_oracle.moe_layer(s["xn"], s["h"], s["w_r"], s["b"], s["wg"], s["wu"], s["wd"], cfg.k,
-                                cfg.score_fn, shared=s["sh"], gamma=cfg.gamma)
+    def __init__(self, cfg, k, n):
+        from oracle import moe_oracle as O
+        self.O, self.cfg, self.k, self.n = O, cfg, k, n
+        xn, h = synth.make_tokens(cfg, "cpu", rows=np.arange(n))
+        self.x = xn.double().numpy()
+        self.h = h.double().numpy()
+        w_r, b = synth.make_router(cfg, "cpu")
+        self.w_r, self.b = w_r.numpy(), b.numpy()
+        # the experts the sample visits (the routing is recomputed, timed, in every run)
+        idx = O.route(self.x, self.w_r, self.b, k, cfg.score_fn)["idx"]
+        self.used = sorted({int(e) for e in idx.ravel()})
+        self.weights = {e: synth.make_expert(cfg, e, "cpu") for e in self.used}
+        self.shared = None
+        if cfg.shared:
+            self.shared = tuple(t.double().numpy() for t in synth.make_expert(cfg, 0, "cpu", shared=True))
+
+    def run(self):
+        """One pass; returns the seconds spent inside the oracle's functions."""
+        O, cfg, k = self.O, self.cfg, self.k
+        clock = time.perf_counter
+        t0 = clock()
+        r = O.route(self.x, self.w_r, self.b, k, cfg.score_fn)
+        counts = O.expert_counts(r["idx"], cfg.E)
+        offsets = O.exclusive_scan(counts)
+        row_map, perm = O.stable_permutation(r["idx"], offsets)
+        x_perm = self.x[perm]
+        y = np.zeros((len(perm), cfg.D))
+        spent = clock() - t0
+        for e in self.used:
+            a, b = int(offsets[e]), int(offsets[e + 1])
+            if b > a:
+                wg, wu, wd = (t.double().numpy() for t in self.weights[e])  # untimed widening
+                t0 = clock()
+                y[a:b] = O.swiglu_expert(x_perm[a:b], wg, wu, wd)
+                spent += clock() - t0
+        t0 = clock()
+        ysh = O.swiglu_expert(self.x, *self.shared) if self.shared else None
+        O.combine(y, row_map, r["gate"], residual=self.h, shared_y=ysh)
+        O.bias_update(self.b, counts, r["idx"].size, cfg.gamma)
+        return spent + clock() - t0
+
+    def describe(self):
+        return (f"first {self.n} of {self.cfg.N} tokens, k={self.k}: the oracle (numpy float64) routes them over "
+                f"all {self.cfg.E} experts and runs the {len(self.used)} experts they visit"
+                + (" and the shared expert" if self.cfg.shared else "")
+                + "; weights regenerated and widened to float64 outside the timed sections")
 
 
 def blas_threads():
@@ -396,44 +576,37 @@ def blas_threads():
         return os.cpu_count() or 1
 
 
-def cpu_baseline(cfg, budget_s=20.0):
-    """The oracle, as it stands, on a bounded token sample of the workload (host cores)."""
-    n = min(cfg.N, 64)
-    s = oracle_sample(cfg, cfg.N)
-    while True:
-        sub = dict(s, xn=s["xn"][:n], h=s["h"][:n])
-        t = time.perf_counter()
-        run_oracle(cfg, sub)
-        dt = time.perf_counter() - t
-        if dt * 2 > budget_s or n >= cfg.N:
-            break
-        n = min(cfg.N, int(n * max(2.0, min(8.0, budget_s / 2 / max(dt, 1e-3)))))
-    return {"value": n / dt, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
-            "sample": f"first {n} of {cfg.N} tokens of the workload, all {cfg.E} experts "
-                      f"(numpy float64, {dt:.1f} s)"}
+def cpu_baseline(cfg, k, budget_s=10.0, max_runs=80):
+    """The oracle, as it stands, on the reference arm's token sample, repeated for about
+    `budget_s` seconds of oracle time (host cores)."""
+    s = OracleSample(cfg, k, min(cfg.N, ORACLE_SAMPLE_TOKENS[cfg.name]))
+    spent, runs = 0.0, 0
+    while runs < max_runs and (spent < budget_s or runs < 2):
+        spent += s.run()
+        runs += 1
+    return {"value": s.n * runs / spent, "unit": "tokens/s", "cores": blas_threads(), "cpu": cpu_model(),
+            "kind": "oracle", "sample": s.describe() + f"; {runs} runs, {spent:.1f} s"}
 
 
-def reference_arm(args, cfg):
+def reference_arm(args, cfg, k):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    s = oracle_sample(cfg, cfg.N)
-    n = min(cfg.N, 128)
-    sub = dict(s, xn=s["xn"][:n], h=s["h"][:n])
+    s = OracleSample(cfg, k, min(cfg.N, ORACLE_SAMPLE_TOKENS[cfg.name]))
     times = []
     for i in range(args.warmup + args.steps):
-        t = time.perf_counter()
-        run_oracle(cfg, sub)
+        dt = s.run()
         if i >= args.warmup:
-            times.append(time.perf_counter() - t)
+            times.append(dt)
     tot = sum(times)
-    val = n * len(times) / tot
+    val = s.n * len(times) / tot
     line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / len(times),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": workload_name(cfg)},
-            "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
-                             "sample": f"first {n} of {cfg.N} tokens per step, all {cfg.E} experts"},
+            "data": "synthetic (seeded SplitMix64 / Irwin-Hall Gaussian tokens and weights)",
+            "config": config_dict(cfg, k, args.gpus),
+            "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": blas_threads(), "cpu": cpu_model(),
+                             "kind": "oracle", "sample": s.describe() + " per step"},
             "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -443,12 +616,14 @@ def reference_arm(args, cfg):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", default="handbook", choices=sorted(synth.CONFIGS))
+    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(synth.CONFIGS))
+    ap.add_argument("--k", type=int, default=0, help="experts per token (default: the configuration's)")
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
-    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true", help="measure the headline workload only")
     rows = ap.add_mutually_exclusive_group()
     rows.add_argument("--permute-copy", action="store_true",
                       help="the permute writes the permuted rows x_perm and GEMM1 loads them by TMA")
@@ -457,8 +632,9 @@ def main():
                            "chooses by size)")
     args = ap.parse_args()
     cfg = synth.CONFIGS[args.config]
+    k = args.k or cfg.k
     if args.impl == "reference":
-        reference_arm(args, cfg)
+        reference_arm(args, cfg, k)
         return
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
@@ -470,76 +646,69 @@ def main():
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
     dev = torch.device("cuda", local)
+    pk, pk_kind = peaks()
+    gather = True if args.gather else (False if args.permute_copy else None)
 
-    step = Step(cfg, dev, rank, world, gather=True if args.gather else (False if args.permute_copy else None))
+    wl = Workload(cfg, k, dev, rank, world, gather=gather)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
-        total_ms, stage_us, launch_mode = time_device(step, args.steps, args.warmup, world)
+        head, total_ms = measure(wl, args.steps, args.warmup, world, pk, args.e2e_steps)
     clocks = clk.summary()
     remeasured = clock_problem(clocks)
     # every rank measures again if any rank's record is invalid (the timing has barriers)
     if max_over_ranks(1.0 if remeasured else 0.0, world) > 0:
         remeasured = remeasured or "another rank's clock record"
         with ClockSampler(local) as clk:
-            total_ms, stage_us, launch_mode = time_device(step, args.steps, args.warmup, world)
+            head, total_ms = measure(wl, args.steps, args.warmup, world, pk, args.e2e_steps)
         clocks = clk.summary()
-    total_ms = max_over_ranks(total_ms, world)
-    st = moe.last_device_status()
-    if st != 0:
-        raise SystemExit(f"device status {moe.STATUS.get(st, st)}")
-    e2e_ms, bi, bo = time_e2e(step, args.e2e_steps, args.warmup, world)
-    e2e_ms = max_over_ranks(e2e_ms, world)
 
-    ms_step = total_ms / args.steps
-    tokens = cfg.N * world
-    value = tokens / (ms_step * 1e-3)
-    alg = algorithmic(cfg, copy_rows=not step.layer.gather)
-    pk, pk_kind = peaks()
-    gemm_us = stage_us["grouped_swiglu"]
-    gemm_tflops = alg["gemm_flops"] / (gemm_us * 1e-6) / 1e12
-    perm_gbs = alg["permute_bytes"] / (stage_us["permute"] * 1e-6) / 1e9
-    # a kernel timed inside a loop of a second or more runs under the power cap: compare it
-    # with the sustained bf16 figure; shorter timed regions with the burst figure
-    long_run = total_ms >= 1000.0
-    peak_t = pk["bf16_tflops_sustained"] if long_run else pk["bf16_tflops"]
-    peak_label = f"{pk_kind} bf16 {'sustained' if long_run else 'burst'}"
+    g = head["grouped_gemm"]
+    gemm_ms = g["us"] * 1e-3
+    roof = {k2: g[k2] for k2 in ("bound", "achieved", "peak", "unit", "frac", "peak_kind")}
+    roof.update({"kernel": f"{g['kernel']} ({g['launches']} launches, one call)",
+                 "traffic": recorded_traffic(cfg, wl.layer.gather), "traffic_unit": "bytes per call (ncu)",
+                 "peak_source": pk_kind, "timed": head["stage_us_from"],
+                 "algorithmic": (f"{g['algorithmic_gb']:.2f} GB" if g["bound"] == "hbm"
+                                 else f"{g['algorithmic_gflop']:.1f} GFLOP") + " per call",
+                 "call_ms": gemm_ms})
     line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "metric": METRIC, "value": head["tokens_per_s"], "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if cfg.dtype == "bf16" else "f32",
         "data": "synthetic (seeded SplitMix64 / Irwin-Hall Gaussian tokens and weights)",
-        "config": {"workload": workload_name(cfg), "tokens_per_gpu": cfg.N,
-                   "l2": "inputs larger than L2: every step streams %.0f MB of expert weights"
-                         % (3 * cfg.E * cfg.D * cfg.F * 2 / 1e6),
-                   "gemm1_rows": "gathered from xn" if step.layer.gather else "permuted copy x_perm",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "launch": launch_mode,
-                   "stage_us_from": "a second pass of the same steps, eager, events between stages"},
-        "roofline": {"kernel": ("moe_grouped_swiglu_gather" if step.layer.gather else "moe_grouped_swiglu")
-                               + " (GEMM1+SwiGLU and GEMM2 launches)", "bound": "tensor",
-                     "achieved": gemm_tflops, "peak": peak_t, "unit": "TFLOP/s",
-                     "frac": gemm_tflops / peak_t, "traffic": recorded_traffic(cfg, step.layer.gather),
-                     "traffic_unit": "bytes per call (ncu)", "peak_kind": peak_label,
-                     "frac_of_burst": gemm_tflops / pk["bf16_tflops"]},
-        "grouped_gemm_tflops": gemm_tflops,
-        # with gathering, the permute moves no rows (GEMM1 reads them): only its index work
-        "permute_gbs": perm_gbs,
-        "permute_frac_hbm": None if step.layer.gather else perm_gbs / pk["hbm_gbs"],
-        "permute_moves_rows": not step.layer.gather,
-        "router_gbs": alg["router_bytes"] / (stage_us["router"] * 1e-6) / 1e9,
-        "combine_gbs": alg["combine_bytes"] / (stage_us["combine"] * 1e-6) / 1e9,
-        "stage_us": {k: round(v, 2) for k, v in stage_us.items()},
-        "gpu_launches": step.launches * args.steps,
+        "config": config_dict(cfg, k, world),
+        "launch": head["launch"], "gemm1_rows": head["gemm1_rows"],
+        "roofline": roof,
+        "grouped_gemm_tflops": g["tflops"],
+        "router": head["router"], "permute": head["permute"], "permute_with_row_copy": head["permute_with_row_copy"],
+        "combine": head["combine"],
+        "stage_us": head["stage_us"], "stage_sum_us": head["stage_sum_us"], "stage_us_from": head["stage_us_from"],
+        "gpu_launches": wl.launches * args.steps,
         "clocks": dict(clocks, remeasured_after=remeasured) if remeasured else clocks,
-        "e2e": {"value": tokens / (e2e_ms / args.e2e_steps * 1e-3), "unit": "tokens/s",
-                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo},
+        "e2e": head["e2e"],
     }
+    if "shared_expert" in head:
+        line["shared_expert"] = head["shared_expert"]
     if rank == 0:
-        line["load_balance"] = load_balance_trace(step)
-        if cfg.name == "skewed":  # serving with fewer experts per token than trained
-            line["serving_fewer_experts"] = time_fewer_experts(step, 4, min(args.steps, 500), args.warmup)
+        line["load_balance"] = load_balance_trace(wl)
+    del wl
+    torch.cuda.empty_cache()
+    if not args.no_per_config:
+        per = {}
+        for label, name, kk in WORKLOADS:
+            c2 = synth.CONFIGS[name]
+            if name == cfg.name and kk == k:
+                continue
+            w2 = Workload(c2, kk, dev, rank, world, gather=gather if c2.dtype == "bf16" else None)
+            r2, _ = measure(w2, args.steps, args.warmup, world, pk, args.e2e_steps)
+            if rank == 0 and c2.bias_steps > 1:
+                r2["load_balance"] = load_balance_trace(w2, c2.bias_steps)
+            per[label] = r2
+            del w2
+            torch.cuda.empty_cache()
+        line["per_config"] = per
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(cfg)
+        line["cpu_baseline"] = cpu_baseline(cfg, k)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
