@@ -31,6 +31,10 @@
  *    moe_last_device_status), so a sequence of calls can be captured in a CUDA graph
  *    once each entry point has run once on the device.
  *  - Results are deterministic: the same inputs give the same bits, run to run.
+ *  - The library looks up the device addresses of its two module-scope device variables
+ *    (the status word, the moe_permute_noalloc scratch) once per device and keeps them
+ *    for the life of the process; a cudaDeviceReset while the library is loaded
+ *    invalidates them and is not supported.
  *  - Kernels are launched with programmatic dependent launch: each may start while the
  *    kernel before it on the stream drains, and waits for that kernel to complete before
  *    it touches global memory, so stream order means what it always does.  MOE_PDL=0 in
@@ -176,13 +180,23 @@ moe_status_t moe_permute(const void* xn, moe_dtype_t dtype, int N, int D,
                          moe_stream_t stream);
 
 /*
+ * moe_expert_capacity -- slots per expert for a capacity factor C.
+ * Lesson "Load-balancing problem" item 2: each expert processes at most a fixed share of
+ * the batch, capacity = C * N / E tokens; read per (token, slot) assignment here:
+ * ceil(C * N * k / E) slots, evaluated in double precision, capped at N * k (a capacity of
+ * N * k already keeps every slot).  Host-only arithmetic; no device, no stream.
+ * Returns -1 for C < 0 (or NaN), N < 0, k < 1 or E < 1.
+ */
+int64_t moe_expert_capacity(double capacity_factor, int N, int k, int E);
+
+/*
  * moe_permute_capacity -- moe_permute with a per-expert capacity (token dropping).
  * Lesson "Load-balancing problem" item 2: each expert processes at most a fixed number of
  * tokens and the overflow skips the layer.  Read here per (token, slot) assignment: an
  * expert keeps the first `capacity` of its slots in slot order n*k + j; every later slot
  * gets row_map = -1, no row and no copy, so moe_unpermute_combine adds nothing for it (the
  * remaining gates are not renormalised).  For a capacity factor C use
- * capacity = ceil(C * N * k / E).
+ * capacity = moe_expert_capacity(C, N, k, E).
  *   counts   [E]     the routed demand (before dropping), which drives moe_bias_update
  *   offsets  [E + 1] exclusive scan of the kept counts min(counts, capacity)
  * Other arguments as moe_permute; perm_token / x_perm hold offsets[E] <= N*k rows.
@@ -206,7 +220,9 @@ moe_status_t moe_permute_capacity(const void* xn, moe_dtype_t dtype, int N, int 
  * moe_permute_noalloc_max_scratch_bytes() bytes (256 KiB), which every GPU that loads
  * the library holds until the process exits.  A size needing more scratch than that
  * (moe_permute_workspace_bytes(N, k, E) larger than the array) is rejected with
- * MOE_ERR_UNSUPPORTED before anything is launched.  No call allocates or frees memory.
+ * MOE_ERR_UNSUPPORTED before anything is launched: the scratch is at most 128 token
+ * chunks of E int32 counters, so every N is accepted while E <= 512, and at E = 1024
+ * batches of at most N = 64 tokens.  No call allocates or frees memory.
  * The first call on a device looks up the array's device address once for that device
  * (a CUDA runtime query); make that first call before any stream capture.  All calls on
  * a device share the one array and nothing in it needs to start at zero; calls that

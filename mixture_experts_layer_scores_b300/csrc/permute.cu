@@ -16,6 +16,8 @@
 //             position < capacity, else -1 (dropped).  Writes row_map and perm_token.
 //   4. copy : grid-stride 16-byte row moves xn[n] -> x_perm[row_map[n, j]], each source
 //             vector read once and written k times.
+#include <cmath>
+
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -218,6 +220,14 @@ extern "C" size_t moe_permute_workspace_bytes(int N, int k, int E) {
   if (N <= 0 || k <= 0 || E <= 0) return 0;
   const moe::Plan p = moe::plan(N);
   return (size_t)p.nb * (size_t)E * sizeof(int32_t);
+}
+
+extern "C" int64_t moe_expert_capacity(double capacity_factor, int N, int k, int E) {
+  if (!(capacity_factor >= 0.0) || N < 0 || k < 1 || E < 1) return -1;
+  // evaluated left to right in double, like ceil(C * N * k / E) written out
+  const double slots = std::ceil(capacity_factor * (double)N * (double)k / (double)E);
+  const int64_t all = (int64_t)N * k;
+  return slots >= (double)all ? all : (int64_t)slots;
 }
 
 extern "C" moe_status_t moe_permute_capacity(const void* xn, moe_dtype_t dtype, int N, int D,

@@ -25,7 +25,7 @@ EXPORTS = ("moe_status_string", "moe_last_device_status", "moe_version", "moe_ro
            "moe_unpermute_combine", "moe_bias_update", "moe_permute_noalloc",
            "moe_permute_noalloc_max_scratch_bytes", "moe_router_split_bytes", "moe_router_split",
            "moe_router_topk_split", "moe_router_topk_split_workspace_bytes", "moe_permute_capacity",
-           "moe_grouped_swiglu_gather", "moe_grouped_swiglu_ex")
+           "moe_grouped_swiglu_gather", "moe_grouped_swiglu_ex", "moe_expert_capacity")
 
 
 class MoEError(RuntimeError):
@@ -66,6 +66,7 @@ def load():
         "moe_router_split": ([vp, i32, i32, vp, vp], i32),
         "moe_router_topk_split": ([vp, i32, i32, vp, vp, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp], i32),
         "moe_router_topk_split_workspace_bytes": ([i32, i32, i32], sz),
+        "moe_expert_capacity": ([ctypes.c_double, i32, i32, i32], i64),
     }
     for name, (args, res) in sig.items():
         f = getattr(L, name)
@@ -208,9 +209,11 @@ def permute_workspace_bytes(N, k, E) -> int:
 
 
 def expert_capacity(capacity_factor, N, k, E) -> int:
-    """Slots per expert for a capacity factor C: ceil(C * N * k / E)."""
-    import math
-    return int(math.ceil(capacity_factor * N * k / E))
+    """Slots per expert for a capacity factor C (moe_expert_capacity)."""
+    c = int(load().moe_expert_capacity(float(capacity_factor), int(N), int(k), int(E)))
+    if c < 0:
+        raise ValueError(f"moe_expert_capacity rejected C={capacity_factor}, N={N}, k={k}, E={E}")
+    return c
 
 
 def moe_permute(xn, topk_idx, E, counts=None, offsets=None, row_map=None, perm_token=None,

@@ -286,7 +286,37 @@ def check_capacity(o):
     assert np.allclose(r["out"], want, rtol=1e-12, atol=1e-12)
 
 
+def check_token_outputs(o):
+    """The layer formula evaluated for a few tokens, one expert at a time (what checks
+    sampled tokens of full-size layers), equals the same formula in torch float64 from the
+    same routing, and the whole layer's output on those tokens (lesson 'Concept' and
+    'Shared experts': out = h + shared(xn) + sum_j gate_j * Expert_j(xn))."""
+    N, D, E, F, k = 12, 16, 6, 10, 3
+    x, h = _rand(91, N, D), _rand(92, N, D)
+    w = _rand(93, E, D)
+    wg, wu, wd = _rand(94, E, F, D, scale=.3), _rand(95, E, F, D, scale=.3), _rand(96, E, D, F, scale=.3)
+    sh = (_rand(97, 1, F, D, scale=.3), _rand(98, 1, F, D, scale=.3), _rand(99, 1, D, F, scale=.3))
+    for fn, shared in (("sigmoid", sh), ("softmax", None)):
+        r = o.moe_layer(x, h, w, None, wg, wu, wd, k, fn, shared=shared)
+        toks = np.array([0, 5, 11])
+        got = o.token_outputs(toks, x[toks], h[toks], r["idx"][toks], r["gate"][toks],
+                              lambda e: (wg[e], wu[e], wd[e]),
+                              shared=None if shared is None else tuple(t[0] for t in shared))
+        t = lambda a: torch.from_numpy(np.asarray(a, np.float64))
+        swiglu = lambda xx, a, b, c: (torch.nn.functional.silu(xx @ t(a).T) * (xx @ t(b).T)) @ t(c).T
+        ref = t(h[toks]).clone()
+        for i, n in enumerate(toks):
+            xx = t(x[n:n + 1])
+            if shared is not None:
+                ref[i] += swiglu(xx, sh[0][0], sh[1][0], sh[2][0])[0]
+            for j in range(k):
+                e = int(r["idx"][n, j])
+                ref[i] += float(r["gate"][n, j]) * swiglu(xx, wg[e], wu[e], wd[e])[0]
+        assert np.allclose(got, ref.numpy(), rtol=1e-12, atol=1e-12), fn
+        assert np.allclose(got, r["out"][toks], rtol=1e-12, atol=1e-12), fn
+
+
 ALL_CHECKS = [check_route_golden, check_layer_golden, check_dense_reduction, check_split_dense,
               check_all_chosen, check_logits_exact, check_library_equivalents,
               check_bruteforce_topk, check_invariants, check_bias_update_rule, check_bias_dynamics,
-              check_capacity]
+              check_capacity, check_token_outputs]

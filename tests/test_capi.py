@@ -5,6 +5,7 @@ import os
 import re
 
 import pytest
+import torch
 
 from mixture_experts_layer_scores_b300 import build, moe
 
@@ -53,6 +54,24 @@ def test_workspace_size(lib):
     assert b > 0 and b % 4 == 0 and b <= 128 * 64 * 4
 
 
+def test_expert_capacity_through_the_abi(lib):
+    """ceil(C N k / E), capped at N k; -1 for arguments outside the domain."""
+    raw = ctypes.CDLL(moe.lib_path())
+    raw.moe_expert_capacity.argtypes = [ctypes.c_double, ctypes.c_int, ctypes.c_int, ctypes.c_int]
+    raw.moe_expert_capacity.restype = ctypes.c_int64
+    cap = raw.moe_expert_capacity
+    assert cap(1.0, 8, 2, 4) == 4            # exactly the uniform share
+    assert cap(1.25, 10, 2, 4) == 7          # 6.25 rounds up
+    assert cap(0.5, 16384, 8, 64) == 1024
+    assert cap(0.0, 100, 2, 8) == 0
+    assert cap(100.0, 10, 2, 4) == 20        # capped at N k
+    assert cap(1.0, 0, 2, 4) == 0
+    assert cap(-1.0, 8, 2, 4) == -1 and cap(float("nan"), 8, 2, 4) == -1
+    assert cap(1.0, -1, 2, 4) == -1 and cap(1.0, 8, 0, 4) == -1 and cap(1.0, 8, 2, 0) == -1
+
+
+@pytest.mark.skipif(torch.cuda.is_available(),
+                    reason="passes placeholder device addresses: a host-only check, never run beside a GPU")
 def test_host_validation_rejects_before_launch(lib):
     vp = ctypes.c_void_p
     # k > E, E too large, D not a multiple of 64, null outputs: no launch happens

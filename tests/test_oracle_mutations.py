@@ -134,10 +134,24 @@ def _inclusive_scan(m):
     m.exclusive_scan = exclusive_scan
 
 
+def _token_outputs_no_shared(m):
+    orig = m.token_outputs
+    def token_outputs(tokens, xn_rows, h_rows, idx_rows, gate_rows, expert_weights, shared=None):
+        return orig(tokens, xn_rows, h_rows, idx_rows, gate_rows, expert_weights, None)
+    m.token_outputs = token_outputs
+
+
+def _token_outputs_gate_of_next_slot(m):
+    orig = m.token_outputs
+    def token_outputs(tokens, xn_rows, h_rows, idx_rows, gate_rows, expert_weights, shared=None):
+        return orig(tokens, xn_rows, h_rows, idx_rows, np.roll(gate_rows, 1, axis=1), expert_weights, shared)
+    m.token_outputs = token_outputs
+
+
 MUTATIONS = [_gates_from_biased, _ties_to_higher_id, _silu_on_up, _no_residual, _no_shared,
              _bias_sign_flipped, _unstable_permutation, _sigmoid_unnormalised,
              _softmax_no_max_subtract_all_experts, _down_transposed_slice, _logits_bf16,
-             _inclusive_scan]
+             _inclusive_scan, _token_outputs_no_shared, _token_outputs_gate_of_next_slot]
 
 
 @pytest.mark.parametrize("mutate", MUTATIONS, ids=lambda f: f.__name__.strip("_"))

@@ -6,8 +6,6 @@ workspace.  moe_permute_noalloc keeps that scratch in a fixed array inside the l
 This file is collected last so that a run stopping at the first failure has already run
 every other test.
 """
-import ctypes
-
 import numpy as np
 import pytest
 import torch
@@ -20,19 +18,25 @@ def test_noalloc_limit_is_stated_and_enforced():
     L = moe.load()
     cap = L.moe_permute_noalloc_max_scratch_bytes()
     assert cap == 256 * 1024
-    # (N, k, E) whose scratch exceeds the array: rejected on the host before any launch
-    N, k, E = 1 << 16, 2, 1024
-    assert L.moe_permute_workspace_bytes(N, k, E) > cap
-    vp = ctypes.c_void_p
-    assert L.moe_permute_noalloc(vp(16), 1, N, 64, vp(16), k, E, vp(16), vp(16), vp(16), vp(16),
-                                 vp(16), None) == -2
+    # Sizes whose scratch exceeds the array are rejected on the host before any launch (and
+    # before any pointer is looked at: every pointer here is NULL).  With at most 128 token
+    # chunks of E int32 counters each, every N fits while E <= 512; at E = 1024 the largest
+    # accepted batch is N = 64 (64 one-token chunks, exactly 256 KiB).
+    for N, k, E in ((1 << 16, 2, 1024), (65, 8, 1024)):
+        assert L.moe_permute_workspace_bytes(N, k, E) > cap
+        assert L.moe_permute_noalloc(None, 1, N, 64, None, k, E, None, None, None, None, None, None) == -2
+    assert L.moe_permute_workspace_bytes(64, 8, 1024) == cap
+    for N in (1, 100, 1 << 20):
+        assert L.moe_permute_workspace_bytes(N, 16, 512) <= cap
 
 
 @pytest.mark.gpu
-def test_noalloc_matches_workspace_entry_point_on_two_calls():
+@pytest.mark.parametrize("N,E,k", [(777, 64, 8), (64, 1024, 8)], ids=["N777-E64", "N64-E1024-full-scratch"])
+def test_noalloc_matches_workspace_entry_point_on_two_calls(N, E, k):
     """Bit-exact agreement with moe_permute on two calls in a row (the second with other
-    routing, so stale scratch from the first call cannot leak into it)."""
-    cfg = synth.scaled(synth.CONFIGS["handbook"], N=777, D=256, E=64, F=128, k=8)
+    routing, so stale scratch from the first call cannot leak into it), at a small size and
+    at the largest size the array holds (E = 1024, N = 64: all 256 KiB in use)."""
+    cfg = synth.scaled(synth.CONFIGS["handbook"], N=N, D=256, E=E, F=128, k=k)
     xn, _ = synth.make_tokens(cfg, "cuda")
     rng = np.random.default_rng(9)
     for call in range(2):
