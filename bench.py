@@ -211,6 +211,7 @@ def cpu_model():
 class Workload:
     """One layer (weights, tokens, reusable buffers) and its step: forward + bias step."""
 
+    # "bias": the separate bias step of replicas (empty on one GPU, where the permute does it)
     STAGES = ("router", "permute", "grouped_swiglu", "shared", "combine", "bias")
 
     def __init__(self, cfg, k, dev, rank=0, world=1, gather=None):
@@ -231,7 +232,9 @@ class Workload:
         rec(0)
         L.route(xn)
         rec(1)
-        L.permute(xn)
+        # one replica: the +-gamma step rides in the permute's launches; replicas sum the
+        # counts first (the global load histogram), then step the bias
+        L.permute(xn, update_bias=self.world == 1)
         rec(2)
         L.experts(xn)
         rec(3)
@@ -239,14 +242,14 @@ class Workload:
         rec(4)
         out = L.combine(h, out=out)
         rec(5)
-        world = moe.global_counts(L.counts)  # global load histogram for the bias step
-        L.bias_step(world)
+        if self.world > 1:
+            L.bias_step(moe.global_counts(L.counts))
         rec(6)
         return out
 
     @property
     def launches(self):
-        return self.layer.kernels_per_forward
+        return self.layer.kernels_per_forward(fused_bias=self.world == 1)
 
 
 def _timed(fn, steps):
@@ -301,7 +304,7 @@ def stage_times(wl, steps, world):
                 wl.run(events=evs[i])
             graphs.append(g)
         torch.cuda.current_stream().wait_stream(s)
-        for g in graphs[:3]:  # warm
+        for g in graphs:  # every graph's first replay happens before the timed pass
             g.replay()
         steps_fn = [g.replay for g in graphs]
         how = "back-to-back replays of CUDA graphs of the step with event nodes between the stages"

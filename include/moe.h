@@ -58,7 +58,7 @@ typedef enum moe_status {
   MOE_ERR_UNSUPPORTED = -2, /* shape or dtype the library does not run */
   MOE_ERR_CUDA = -3,        /* a CUDA runtime call or kernel launch failed */
   MOE_ERR_TIMEOUT = -4,     /* a device-side wait gave up (status word) */
-  MOE_ERR_NAN_INPUT = -5    /* reserved for input screening */
+  MOE_ERR_NAN_INPUT = -5    /* a router logit was NaN or infinite (status word) */
 } moe_status_t;
 
 typedef enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype_t;
@@ -85,11 +85,29 @@ typedef enum moe_score_fn {
 /* Human-readable name of a status code (static string, never NULL). */
 const char* moe_status_string(moe_status_t status);
 
-/* Waits for `stream`, then returns and clears the status word of the current device:
- * MOE_OK, MOE_ERR_TIMEOUT (a pipeline wait gave up) or MOE_ERR_INVALID_ARG (an
- * expert id outside [0, E) reached moe_permute, or a token index outside [0, N)
- * reached moe_grouped_swiglu_gather). */
+/* Waits for `stream`, then returns and clears the status word of the current device.
+ * The first that applies, in this order: MOE_ERR_TIMEOUT (a pipeline wait gave up),
+ * MOE_ERR_INVALID_ARG (an expert id outside [0, E) reached moe_permute, or a token index
+ * outside [0, N) reached moe_grouped_swiglu_gather), MOE_ERR_NAN_INPUT (a router logit
+ * was NaN or infinite, so that token's gates are undefined), MOE_OK. */
 moe_status_t moe_last_device_status(moe_stream_t stream);
+
+/*
+ * moe_selftest_bounded_wait -- run the failure-detection path of the library's pipelines.
+ * No passage of the pages defines this call: it is a diagnostic.  Every tensor-core kernel
+ * waits on its pipeline barriers with a bounded wait (about 2 s of SM cycles); when one runs
+ * out, the kernel records MOE_ERR_TIMEOUT in the status word, lets the copies it started
+ * land, frees its tensor memory and returns, so the context stays usable.  This call
+ * launches one small kernel that waits, with the same code, on a barrier nothing arrives
+ * on, using a limit of `limit_cycles` SM cycles (1000 .. the normal limit), next to a real
+ * 4 KB bulk copy from `src` (a 16-byte-aligned device buffer of at least 4096 bytes) and a
+ * second waiter.  Afterwards moe_last_device_status returns MOE_ERR_TIMEOUT and
+ * steps_out[0] (device int32) is 15: the copy landed (1), the short wait gave up (2), the
+ * second waiter left on the abort flag (4), and the kernel ended with its tensor memory
+ * freed (8).  MOE_ERR_INVALID_ARG for a null or unaligned pointer or a limit out of range.
+ */
+moe_status_t moe_selftest_bounded_wait(const void* src, long long limit_cycles, int32_t* steps_out,
+                                       moe_stream_t stream);
 
 /* Library version, major*10000 + minor*100 + patch. */
 int moe_version(void);
@@ -112,6 +130,8 @@ int moe_version(void);
  * Requires 1 <= k <= min(E, 16), 1 <= E <= 256, D % 64 == 0, N >= 0.
  * Logits are accumulated in fp32 with per-32-element partial sums combined by
  * compensated (two-sum) addition.  (CUDA cores; see moe_router_topk_split for bf16.)
+ * A NaN or infinite logit sets MOE_ERR_NAN_INPUT in the status word (the token is still
+ * routed by the order rule above; its gates are undefined).
  */
 moe_status_t moe_router_topk(const void* xn, moe_dtype_t x_dtype, int N, int D,
                              const float* w_router, const float* bias, int E, int k,
@@ -207,6 +227,25 @@ moe_status_t moe_permute_capacity(const void* xn, moe_dtype_t dtype, int N, int 
                                   int32_t* counts, int32_t* offsets, int32_t* row_map,
                                   int32_t* perm_token, void* x_perm, void* workspace,
                                   size_t workspace_bytes, moe_stream_t stream);
+
+/*
+ * moe_permute_update_bias -- moe_permute_capacity, then the +-gamma bias step on the counts
+ * it has just made, in the same launches (lesson "Build it" step 2: the firing counts of a
+ * step drive the step's bias update; "Load-balancing problem" item 3: the bias only ever
+ * changes which experts are chosen, so moving it once the step's routing is done is the
+ * same as moving it after the whole forward).  Equivalent to moe_permute_capacity followed
+ * by moe_bias_update(counts, E, N * k, gamma, bias, max_over_mean_out).
+ *   gamma, bias [E] (fp32, in place, required), max_over_mean_out [1] (or NULL): as
+ *   moe_bias_update; every other argument as moe_permute_capacity (capacity >= N * k keeps
+ *   every slot).  With data-parallel replicas use moe_permute and, after summing the counts
+ *   across replicas, moe_bias_update instead.
+ */
+moe_status_t moe_permute_update_bias(const void* xn, moe_dtype_t dtype, int N, int D,
+                                     const int32_t* topk_idx, int k, int E, int capacity,
+                                     int32_t* counts, int32_t* offsets, int32_t* row_map,
+                                     int32_t* perm_token, void* x_perm, void* workspace,
+                                     size_t workspace_bytes, float gamma, float* bias,
+                                     float* max_over_mean_out, moe_stream_t stream);
 
 /*
  * moe_permute_noalloc -- moe_permute without a caller-supplied workspace.

@@ -47,6 +47,7 @@ extern "C" moe_status_t moe_last_device_status(moe_stream_t stream) {
   if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
   if (host & moe::kStatusTimeout) return MOE_ERR_TIMEOUT;
   if (host & (moe::kStatusBadExpertId | moe::kStatusBadToken)) return MOE_ERR_INVALID_ARG;
+  if (host & moe::kStatusNonFiniteLogit) return MOE_ERR_NAN_INPUT;
   return MOE_OK;
 }
 

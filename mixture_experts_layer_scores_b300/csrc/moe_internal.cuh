@@ -13,7 +13,7 @@
 namespace moe {
 
 // Device status word values (bit flags, OR-ed by kernels).
-enum : int { kStatusTimeout = 1, kStatusBadExpertId = 2, kStatusBadToken = 4 };
+enum : int { kStatusTimeout = 1, kStatusBadExpertId = 2, kStatusBadToken = 4, kStatusNonFiniteLogit = 8 };
 
 // Address of the current device's status word (set up once per device).
 int* device_status_word();

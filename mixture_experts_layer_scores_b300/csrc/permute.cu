@@ -9,7 +9,8 @@
 //   1. hist : block b counts the ids of its slot chunk in shared memory -> ws[b][E]
 //   2. scan : one block turns ws into per-chunk positions (slots of expert e in earlier
 //             chunks), writes counts (the routed demand) and offsets (exclusive scan of
-//             the kept counts min(count, capacity))
+//             the kept counts min(count, capacity)) and, when asked, applies the +-gamma
+//             bias step to those counts (moe_permute_update_bias)
 //   3. rank : block b walks its chunk in slot order; __match_any_sync gives each slot
 //             its rank among same-expert slots of the warp, a per-warp table orders the
 //             warps; position = chunk position + rank, row = offsets[e] + position while
@@ -58,10 +59,35 @@ __global__ void __launch_bounds__(256) hist_kernel(const int32_t* __restrict__ i
   for (int e = threadIdx.x; e < E; e += blockDim.x) ws[(size_t)blockIdx.x * E + e] = sh[e];
 }
 
+// The +-gamma step on this call's counts (lesson "Load-balancing problem" item 3):
+// bias[e] += gamma * sign(total/E - c_e), the sign taken exactly on integers; and the
+// max/mean load.  Called by every thread of one block with the block's counts in `cnt`.
+__device__ __forceinline__ void bias_step_block(const int* cnt, int E, long long total, float gamma,
+                                                float* __restrict__ bias, float* __restrict__ mom, int* red) {
+  int m = 0;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const long long c = cnt[e];
+    const long long d = total - (long long)E * c;
+    const float sg = d > 0 ? 1.f : (d < 0 ? -1.f : 0.f);
+    if (bias) bias[e] = bias[e] + gamma * sg;
+    m = max(m, (int)c);
+  }
+  if (!mom) return;
+  for (int off = 16; off > 0; off >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, off));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int mm = 0;
+    for (int w = 0; w < (int)(blockDim.x + 31) / 32; ++w) mm = max(mm, red[w]);
+    *mom = total > 0 ? (float)((double)mm * E / (double)total) : 0.f;
+  }
+}
+
 // One block of 1024 threads, E <= 1024.  Thread (g, e) owns expert e over chunk range g.
 __global__ void __launch_bounds__(1024) scan_kernel(int32_t* __restrict__ ws, int nb, int E, int capacity,
                                                     int32_t* __restrict__ counts,
-                                                    int32_t* __restrict__ offsets) {
+                                                    int32_t* __restrict__ offsets, long long total, float gamma,
+                                                    float* __restrict__ bias, float* __restrict__ mom) {
   extern __shared__ int sh[];  // part[P][E], cnt[E], wsum[32]
   const int P = blockDim.x / E;
   int* part = sh;
@@ -123,6 +149,10 @@ __global__ void __launch_bounds__(1024) scan_kernel(int32_t* __restrict__ ws, in
       ws[(size_t)b * E + e] = base;
       base += x;
     }
+  }
+  if (bias || mom) {  // the +-gamma step on these counts (every thread of the block)
+    __syncthreads();
+    bias_step_block(cnt, E, total, gamma, bias, mom, wsum);
   }
 }
 
@@ -230,22 +260,25 @@ extern "C" int64_t moe_expert_capacity(double capacity_factor, int N, int k, int
   return slots >= (double)all ? all : (int64_t)slots;
 }
 
-extern "C" moe_status_t moe_permute_capacity(const void* xn, moe_dtype_t dtype, int N, int D,
-                                             const int32_t* topk_idx, int k, int E, int capacity,
-                                             int32_t* counts, int32_t* offsets, int32_t* row_map,
-                                             int32_t* perm_token, void* x_perm, void* workspace,
-                                             size_t workspace_bytes, moe_stream_t stream) {
-  using namespace moe;
+namespace moe {
+namespace {
+
+// Every permute entry point: histogram, scan, ranks, and the row copy when x_perm is given;
+// with `bias` or `mom`, the +-gamma step on this call's counts as well.
+moe_status_t permute_impl(const void* xn, moe_dtype_t dtype, int N, int D, const int32_t* topk_idx, int k, int E,
+                          int capacity, int32_t* counts, int32_t* offsets, int32_t* row_map, int32_t* perm_token,
+                          void* x_perm, void* workspace, size_t workspace_bytes, float gamma, float* bias,
+                          float* mom, cudaStream_t s) {
   if (N < 0 || k < 1 || E < 1 || k > E || D <= 0 || capacity < 0) return MOE_ERR_INVALID_ARG;
   if (E > 1024 || (long long)N * k >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
   if (dtype != MOE_BF16 && dtype != MOE_F32) return MOE_ERR_UNSUPPORTED;
   if (!counts || !offsets) return MOE_ERR_INVALID_ARG;
   if ((row_map == nullptr) != (perm_token == nullptr)) return MOE_ERR_INVALID_ARG;
   if (x_perm && (!row_map || !xn)) return MOE_ERR_INVALID_ARG;
-  cudaStream_t s = as_cuda(stream);
   if (N == 0) {
     if (cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, s) != cudaSuccess) return MOE_ERR_CUDA;
     if (cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (E + 1), s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (bias || mom) return moe_bias_update(counts, E, 0, gamma, bias, mom, reinterpret_cast<moe_stream_t>(s));
     return MOE_OK;
   }
   if (!topk_idx || !workspace) return MOE_ERR_INVALID_ARG;
@@ -264,7 +297,7 @@ extern "C" moe_status_t moe_permute_capacity(const void* xn, moe_dtype_t dtype, 
   if (st != MOE_OK) return st;
   const int P = 1024 / E;
   st = launch_kernel(scan_kernel, dim3(1), dim3(1024), (size_t)(P * E + E + 32) * sizeof(int), s, ws, p.nb, E,
-                     capacity, counts, offsets);
+                     capacity, counts, offsets, (long long)R, gamma, bias, mom);
   if (st != MOE_OK) return st;
   if (row_map) {
     st = launch_kernel(rank_kernel, dim3(p.nb), dim3(256), (size_t)9 * E * sizeof(int), s, topk_idx, R, k, E, C,
@@ -282,6 +315,29 @@ extern "C" moe_status_t moe_permute_capacity(const void* xn, moe_dtype_t dtype, 
                          static_cast<const int32_t*>(row_map), static_cast<uint4*>(x_perm));
   }
   return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" moe_status_t moe_permute_capacity(const void* xn, moe_dtype_t dtype, int N, int D,
+                                             const int32_t* topk_idx, int k, int E, int capacity,
+                                             int32_t* counts, int32_t* offsets, int32_t* row_map,
+                                             int32_t* perm_token, void* x_perm, void* workspace,
+                                             size_t workspace_bytes, moe_stream_t stream) {
+  return moe::permute_impl(xn, dtype, N, D, topk_idx, k, E, capacity, counts, offsets, row_map, perm_token, x_perm,
+                           workspace, workspace_bytes, 0.f, nullptr, nullptr, moe::as_cuda(stream));
+}
+
+extern "C" moe_status_t moe_permute_update_bias(const void* xn, moe_dtype_t dtype, int N, int D,
+                                                const int32_t* topk_idx, int k, int E, int capacity,
+                                                int32_t* counts, int32_t* offsets, int32_t* row_map,
+                                                int32_t* perm_token, void* x_perm, void* workspace,
+                                                size_t workspace_bytes, float gamma, float* bias,
+                                                float* max_over_mean_out, moe_stream_t stream) {
+  if (!bias) return MOE_ERR_INVALID_ARG;
+  return moe::permute_impl(xn, dtype, N, D, topk_idx, k, E, capacity, counts, offsets, row_map, perm_token, x_perm,
+                           workspace, workspace_bytes, gamma, bias, max_over_mean_out, moe::as_cuda(stream));
 }
 
 extern "C" moe_status_t moe_permute(const void* xn, moe_dtype_t dtype, int N, int D,

@@ -263,7 +263,7 @@ template <int PER>
 __global__ void __launch_bounds__(256) topk_kernel(float* __restrict__ logits, const float* __restrict__ partials,
                                                    int nsplit, const float* __restrict__ bias, int N, int E, int k,
                                                    int score_fn, int32_t* __restrict__ idx, float* __restrict__ gate,
-                                                   uint8_t* __restrict__ tie) {
+                                                   uint8_t* __restrict__ tie, int* __restrict__ status) {
   const int lane = threadIdx.x & 31;
   const int n = blockIdx.x * 8 + (threadIdx.x >> 5);
   grid_dep_wait();
@@ -294,7 +294,7 @@ __global__ void __launch_bounds__(256) topk_kernel(float* __restrict__ logits, c
     }
   }
   warp_topk_gates<PER>(lg, lane, E, k, bias, score_fn, idx + (size_t)n * k, gate + (size_t)n * k,
-                       tie ? tie + n : nullptr);
+                       tie ? tie + n : nullptr, status);
 }
 
 template <int NT>
@@ -383,7 +383,7 @@ extern "C" moe_status_t moe_router_topk_split(const void* xn, int N, int D, cons
   const int grid = (N + 7) / 8;
   auto topk = [&](auto kern) {
     return launch_kernel(kern, dim3(grid), dim3(256), 0, s, logits_out, static_cast<const float*>(part), p.nsplit,
-                         bias, N, E, k, sig, topk_idx, topk_gate, near_tie);
+                         bias, N, E, k, sig, topk_idx, topk_gate, near_tie, status);
   };
   if (E <= 32) return topk(rtc::topk_kernel<1>);
   if (E <= 64) return topk(rtc::topk_kernel<2>);

@@ -95,7 +95,8 @@ template <typename XT, int EP, int TM, int TE>
 __global__ void __launch_bounds__(NT) router_topk_kernel(
     const XT* __restrict__ xn, const float* __restrict__ w, const float* __restrict__ bias,
     int N, int D, int E, int k, int score_fn, float* __restrict__ logits_out,
-    int32_t* __restrict__ topk_idx, float* __restrict__ topk_gate, uint8_t* __restrict__ near_tie) {
+    int32_t* __restrict__ topk_idx, float* __restrict__ topk_gate, uint8_t* __restrict__ near_tie,
+    int* __restrict__ status) {
   constexpr int TGE = EP / TE;  // threads along experts
   static_assert(TGE * (BT / TM) == NT, "thread tile");
   extern __shared__ __align__(16) float smem[];
@@ -192,13 +193,13 @@ __global__ void __launch_bounds__(NT) router_topk_kernel(
 #pragma unroll
     for (int i = 0; i < PER; ++i) lg[i] = lt[nl * (EP + 1) + lane + 32 * i];
     warp_topk_gates<PER>(lg, lane, E, k, bias, score_fn, topk_idx + (size_t)n * k,
-                         topk_gate + (size_t)n * k, near_tie ? near_tie + n : nullptr);
+                         topk_gate + (size_t)n * k, near_tie ? near_tie + n : nullptr, status);
   }
 }
 
 template <typename XT, int EP, int TM, int TE>
 moe_status_t launch(const void* xn, int N, int D, const float* w, const float* bias, int E, int k,
-                    int score_fn, float* logits, int32_t* idx, float* gate, uint8_t* tie,
+                    int score_fn, float* logits, int32_t* idx, float* gate, uint8_t* tie, int* status,
                     cudaStream_t s) {
   const size_t smem = (size_t)(2 * BK * BT + 2 * BK * EP) * sizeof(float);
   auto kern = router_topk_kernel<XT, EP, TM, TE>;
@@ -206,17 +207,17 @@ moe_status_t launch(const void* xn, int N, int D, const float* w, const float* b
     return MOE_ERR_CUDA;
   const int grid = (N + BT - 1) / BT;
   return launch_kernel(kern, dim3(grid), dim3(NT), smem, s, static_cast<const XT*>(xn), w, bias, N, D, E, k,
-                       score_fn, logits, idx, gate, tie);
+                       score_fn, logits, idx, gate, tie, status);
 }
 
 template <typename XT>
 moe_status_t dispatch(const void* xn, int N, int D, const float* w, const float* bias, int E, int k,
-                      int score_fn, float* logits, int32_t* idx, float* gate, uint8_t* tie,
+                      int score_fn, float* logits, int32_t* idx, float* gate, uint8_t* tie, int* status,
                       cudaStream_t s) {
-  if (E <= 32) return launch<XT, 32, 2, 2>(xn, N, D, w, bias, E, k, score_fn, logits, idx, gate, tie, s);
-  if (E <= 64) return launch<XT, 64, 2, 4>(xn, N, D, w, bias, E, k, score_fn, logits, idx, gate, tie, s);
-  if (E <= 128) return launch<XT, 128, 4, 4>(xn, N, D, w, bias, E, k, score_fn, logits, idx, gate, tie, s);
-  return launch<XT, 256, 4, 8>(xn, N, D, w, bias, E, k, score_fn, logits, idx, gate, tie, s);
+  if (E <= 32) return launch<XT, 32, 2, 2>(xn, N, D, w, bias, E, k, score_fn, logits, idx, gate, tie, status, s);
+  if (E <= 64) return launch<XT, 64, 2, 4>(xn, N, D, w, bias, E, k, score_fn, logits, idx, gate, tie, status, s);
+  if (E <= 128) return launch<XT, 128, 4, 4>(xn, N, D, w, bias, E, k, score_fn, logits, idx, gate, tie, status, s);
+  return launch<XT, 256, 4, 8>(xn, N, D, w, bias, E, k, score_fn, logits, idx, gate, tie, status, s);
 }
 
 }  // namespace
@@ -235,10 +236,12 @@ extern "C" moe_status_t moe_router_topk(const void* xn, moe_dtype_t x_dtype, int
   if (!xn || !w_router || !topk_idx || !topk_gate) return MOE_ERR_INVALID_ARG;
   if (!aligned16(xn) || !aligned16(w_router)) return MOE_ERR_INVALID_ARG;
   const int sig = (int)fn;  // score function code
+  int* status = device_status_word();
+  if (!status) return MOE_ERR_CUDA;
   cudaStream_t s = as_cuda(stream);
   if (x_dtype == MOE_BF16)
     return dispatch<__nv_bfloat16>(xn, N, D, w_router, bias, E, k, sig, logits_out, topk_idx,
-                                   topk_gate, near_tie, s);
+                                   topk_gate, near_tie, status, s);
   return dispatch<float>(xn, N, D, w_router, bias, E, k, sig, logits_out, topk_idx, topk_gate,
-                         near_tie, s);
+                         near_tie, status, s);
 }

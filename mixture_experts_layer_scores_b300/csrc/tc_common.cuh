@@ -46,11 +46,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Bounded wait.  Returns false if the kernel is aborting (honour_abort) or the wait
-// exceeded WAIT_LIMIT_CYCLES SM clocks (about 2 s at B300 clocks), in which case it
-// raises the abort flag and the status word.  The limit uses the per-SM cycle counter,
-// a register read, so polling costs nothing extra.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          int* status, bool honour_abort) {
+// exceeded `limit` SM clocks, in which case it raises the abort flag and the status word.
+// The limit uses the per-SM cycle counter, a register read, so polling costs nothing extra.
+__device__ __forceinline__ bool mbar_wait_limit(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                                int* status, bool honour_abort, long long limit) {
   auto poll = [&]() { return mbar_try_wait(bar, parity); };
   if (poll()) return true;
   const long long t0 = clock64();
@@ -58,13 +57,19 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     if (poll()) return true;
     if ((it & 63u) == 0) {
       if (honour_abort && *abort_flag) return false;
-      if (clock64() - t0 > WAIT_LIMIT_CYCLES) {
+      if (clock64() - t0 > limit) {
         *abort_flag = 1;
         atomicOr(status, kStatusTimeout);
         return false;
       }
     }
   }
+}
+
+// The wait every pipeline of the library uses: WAIT_LIMIT_CYCLES (about 2 s at B300 clocks).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          int* status, bool honour_abort) {
+  return mbar_wait_limit(bar, parity, abort_flag, status, honour_abort, WAIT_LIMIT_CYCLES);
 }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,

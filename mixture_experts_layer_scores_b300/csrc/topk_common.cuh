@@ -22,12 +22,18 @@ __device__ __forceinline__ float router_score(float l, int fn) {
 }
 
 // lg[i] = logit of expert lane + 32 i for this warp's token (entries with id >= E ignored).
-// Lane j < k writes idx_row[j] / gate_row[j]; lane 0 writes *tie_out (if non-null).
+// Lane j < k writes idx_row[j] / gate_row[j]; lane 0 writes *tie_out (if non-null).  A NaN or
+// infinite logit (the gates are then undefined) sets kStatusNonFiniteLogit in *status; the
+// selection still follows the order rule (NaN scores last).
 template <int PER>
 __device__ __forceinline__ void warp_topk_gates(const float (&lg)[PER], int lane, int E, int k,
                                                 const float* __restrict__ bias, int score_fn,
                                                 int32_t* __restrict__ idx_row, float* __restrict__ gate_row,
-                                                uint8_t* __restrict__ tie_out) {
+                                                uint8_t* __restrict__ tie_out, int* __restrict__ status) {
+  bool nonfinite = false;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) nonfinite |= (lane + 32 * i < E) && !isfinite(lg[i]);
+  if (__any_sync(0xffffffffu, nonfinite) && lane == 0) atomicOr(status, kStatusNonFiniteLogit);
   float v[PER];
 #pragma unroll
   for (int i = 0; i < PER; ++i) {

@@ -25,7 +25,8 @@ EXPORTS = ("moe_status_string", "moe_last_device_status", "moe_version", "moe_ro
            "moe_unpermute_combine", "moe_bias_update", "moe_permute_noalloc",
            "moe_permute_noalloc_max_scratch_bytes", "moe_router_split_bytes", "moe_router_split",
            "moe_router_topk_split", "moe_router_topk_split_workspace_bytes", "moe_permute_capacity",
-           "moe_grouped_swiglu_gather", "moe_grouped_swiglu_ex", "moe_expert_capacity")
+           "moe_grouped_swiglu_gather", "moe_grouped_swiglu_ex", "moe_expert_capacity",
+           "moe_selftest_bounded_wait", "moe_permute_update_bias")
 
 
 class MoEError(RuntimeError):
@@ -67,6 +68,9 @@ def load():
         "moe_router_topk_split": ([vp, i32, i32, vp, vp, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp], i32),
         "moe_router_topk_split_workspace_bytes": ([i32, i32, i32], sz),
         "moe_expert_capacity": ([ctypes.c_double, i32, i32, i32], i64),
+        "moe_selftest_bounded_wait": ([vp, ctypes.c_longlong, vp, vp], i32),
+        "moe_permute_update_bias": ([vp, i32, i32, i32, vp, i32, i32, i32, vp, vp, vp, vp, vp, vp, sz, f32, vp,
+                                     vp, vp], i32),
     }
     for name, (args, res) in sig.items():
         f = getattr(L, name)
@@ -123,6 +127,18 @@ def last_device_status(stream=None) -> int:
 
 def version() -> int:
     return load().moe_version()
+
+
+def selftest_bounded_wait(src, steps_out, limit_cycles=2_000_000, stream=None):
+    """Launch the library's bounded-wait self-test (moe_selftest_bounded_wait): `src` is a
+    device buffer of at least 4096 bytes, `steps_out` a device int32[1].  Read the timeout
+    it records with last_device_status()."""
+    _need("steps_out", steps_out, torch.int32, (1,))
+    _cuda(src, steps_out)
+    if src.numel() * src.element_size() < 4096:
+        raise ValueError("src: at least 4096 bytes")
+    _chk("moe_selftest_bounded_wait", load().moe_selftest_bounded_wait(
+        _p(src), int(limit_cycles), _p(steps_out), _stream(stream)))
 
 
 def moe_router_topk(xn, w_router, bias, k, score_fn="softmax", logits_out=None, topk_idx=None,
@@ -217,8 +233,11 @@ def expert_capacity(capacity_factor, N, k, E) -> int:
 
 
 def moe_permute(xn, topk_idx, E, counts=None, offsets=None, row_map=None, perm_token=None,
-                x_perm=None, workspace=None, rows=True, copy=True, capacity=None, stream=None):
+                x_perm=None, workspace=None, rows=True, copy=True, capacity=None, stream=None,
+                bias_step=None):
     """Histogram + scan + stable permutation (with an optional per-expert capacity).
+    bias_step = (gamma, bias, max_over_mean or None): also apply the +-gamma step to `bias`
+    from this call's counts (moe_permute_update_bias).
     Returns (counts, offsets, row_map, perm_token, x_perm)."""
     L = load()
     N, k = topk_idx.shape
@@ -247,7 +266,17 @@ def moe_permute(xn, topk_idx, E, counts=None, offsets=None, row_map=None, perm_t
         workspace = torch.empty(max(1, permute_workspace_bytes(N, k, E)), dtype=torch.uint8, device=dev)
     dt = _dt(xn) if xn is not None else MOE_BF16
     _cuda(xn, topk_idx, counts, offsets, row_map, perm_token, x_perm, workspace)
-    if capacity is None:
+    if bias_step is not None:
+        gamma, bias, mom = bias_step
+        _need("bias", bias, torch.float32, (E,), dev)
+        _need("max_over_mean", mom, torch.float32, (1,), dev)
+        _cuda(bias, mom)
+        _chk("moe_permute_update_bias", L.moe_permute_update_bias(
+            _p(xn) if copy else None, dt, N, D, _p(topk_idx), k, E,
+            int(capacity) if capacity is not None else N * k, _p(counts), _p(offsets), _p(row_map),
+            _p(perm_token), _p(x_perm) if copy else None, _p(workspace),
+            workspace.numel() * workspace.element_size(), float(gamma), _p(bias), _p(mom), _stream(stream)))
+    elif capacity is None:
         _chk("moe_permute", L.moe_permute(
             _p(xn) if copy else None, dt, N, D, _p(topk_idx), k, E, _p(counts), _p(offsets),
             _p(row_map), _p(perm_token), _p(x_perm) if copy else None, _p(workspace),
@@ -452,16 +481,15 @@ class MoELayer:
             self.sh_y = None
 
     def forward(self, xn, h, update_bias=True, stream=None, out=None):
-        """out = h + shared(xn) + sum_j gate_j Expert_j(xn); then the +-gamma bias step.
-        Writes self.out, or `out` ([N, D], layer dtype) when given, and returns it."""
+        """out = h + shared(xn) + sum_j gate_j Expert_j(xn), and the +-gamma bias step on
+        this forward's counts (made by the permute's own launches; the bias only affects the
+        next forward's routing).  Writes self.out, or `out` ([N, D], layer dtype) when given,
+        and returns it."""
         self.route(xn, stream)
-        self.permute(xn, stream)
+        self.permute(xn, stream, update_bias=update_bias)
         self.experts(xn, stream)
         self.shared_expert(xn, stream)
-        out = self.combine(h, stream, out)
-        if update_bias:
-            self.bias_step(1, stream)
-        return out
+        return self.combine(h, stream, out)
 
     def capture(self, xn, h, update_bias=True, out=None):
         """Record one forward on the fixed buffers xn and h (writing self.out, or `out`) as a
@@ -483,11 +511,14 @@ class MoELayer:
         torch.cuda.current_stream().wait_stream(s)
         return g.replay
 
-    def permute(self, xn, stream=None):
-        """Histogram, scan, stable permutation (and the row copy unless gathering)."""
+    def permute(self, xn, stream=None, update_bias=False):
+        """Histogram, scan, stable permutation (and the row copy unless gathering); with
+        update_bias, the +-gamma step on these counts in the same launches.  Data-parallel
+        replicas leave update_bias off and call bias_step after summing the counts."""
         moe_permute(xn, self.idx, self.E, self.counts, self.offsets, self.row_map,
                     self.perm_token, self.x_perm, self.workspace, copy=not self.gather,
-                    capacity=self.capacity, stream=stream)
+                    capacity=self.capacity, stream=stream,
+                    bias_step=(self.gamma, self.w.bias, self.mom) if update_bias else None)
 
     def experts(self, xn, stream=None):
         """Every routed expert's SwiGLU FFN over its block of permuted rows -> y_perm."""
@@ -528,8 +559,9 @@ class MoELayer:
             moe_router_topk(xn, w.w_router, w.bias, self.k, self.score_fn, self.logits, self.idx,
                             self.gate, self.near_tie, stream=stream)
 
-    @property
-    def kernels_per_forward(self):
+    def kernels_per_forward(self, fused_bias=True):
+        """Kernel launches of one forward (+ bias step, fused into the permute or not)."""
         router = 3 if self.tc_router else 1
-        permute = 3 if self.gather else 4
-        return router + permute + 2 + (2 if self.w.shared else 0) + 1 + 1
+        permute = 3 + (0 if self.gather else 1)  # histogram, scan (+ bias step), rank (+ row copy)
+        bias = 0 if fused_bias else 1
+        return router + permute + 2 + (2 if self.w.shared else 0) + 1 + bias

@@ -28,15 +28,28 @@ def test_algorithmic_work_matches_closed_forms():
     assert d["shared_flops"] == 6 * 4096 * 7168 * 2048
 
 
+SRCS = ["mixture_experts_layer_scores_b300/csrc/grouped_swiglu.cu",
+        "mixture_experts_layer_scores_b300/csrc/tc_common.cuh",
+        "mixture_experts_layer_scores_b300/csrc/moe_internal.cuh"]
+
+
 def _tree(tmp, alter=None):
-    srcs = ["mixture_experts_layer_scores_b300/csrc/grouped_swiglu.cu",
-            "mixture_experts_layer_scores_b300/csrc/tc_common.cuh",
-            "mixture_experts_layer_scores_b300/csrc/moe_internal.cuh"]
-    for rel in srcs + ["profiles/grouped_gemm_handbook_traffic.txt",
-                       "profiles/grouped_gemm_handbook_gather_traffic.txt"]:
+    """A copy of the GEMM sources with traffic records written for them (hash of the copies),
+    then optionally one source changed after the records were taken."""
+    import hashlib
+    for rel in SRCS:
         dst = os.path.join(tmp, rel)
         os.makedirs(os.path.dirname(dst), exist_ok=True)
         shutil.copy(os.path.join(ROOT, rel), dst)
+    h = hashlib.sha256()
+    for rel in SRCS:
+        with open(os.path.join(tmp, rel), "rb") as f:
+            h.update(f.read())
+    os.makedirs(os.path.join(tmp, "profiles"), exist_ok=True)
+    for suffix, nbytes in (("", 1500000000), ("_gather", 1400000000)):
+        with open(os.path.join(tmp, "profiles", f"grouped_gemm_handbook{suffix}_traffic.txt"), "w") as f:
+            f.write(f"# test record\nsources={' '.join(SRCS)}\nsources_sha256={h.hexdigest()}\n"
+                    f"dram_bytes_per_call={nbytes}\n")
     if alter:
         with open(os.path.join(tmp, alter), "a") as f:
             f.write("\n// changed\n")
@@ -48,7 +61,7 @@ def test_traffic_record_holds_only_for_the_recorded_sources(tmp_path, monkeypatc
     _tree(str(changed), alter="mixture_experts_layer_scores_b300/csrc/grouped_swiglu.cu")
     monkeypatch.setattr(bench, "ROOT", str(same))
     gather, copy = bench.recorded_traffic(C["handbook"], True), bench.recorded_traffic(C["handbook"], False)
-    assert gather and copy and gather != copy
+    assert (gather, copy) == (1400000000, 1500000000)
     assert bench.recorded_traffic(C["mixtral"], False) is None  # no record for that workload
     monkeypatch.setattr(bench, "ROOT", str(changed))
     assert bench.recorded_traffic(C["handbook"], True) is None

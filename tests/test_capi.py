@@ -112,6 +112,9 @@ def test_host_validation_rejects_before_launch(lib):
     # combine: k too large; bias: null counts
     assert lib.moe_unpermute_combine(vp(16), vp(16), vp(16), 4, 17, 64, None, None, vp(16), 1, None) == -2
     assert lib.moe_bias_update(None, 8, 64, ctypes.c_float(1e-3), vp(16), None, None) == -1
+    # bounded-wait self-test: null source, limit outside [1000, normal limit]
+    assert lib.moe_selftest_bounded_wait(None, 2_000_000, vp(16), None) == -1
+    assert lib.moe_selftest_bounded_wait(vp(16), 10, vp(16), None) == -1
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):

@@ -338,3 +338,30 @@ def test_combine_chunks_and_dropped_slots(name):
                              residual=None if res is None else P.np64(res),
                              shared_y=None if shared is None else P.np64(shared))
     P.assert_close(name, P.np64(out.cpu()), ref, f32=dt == torch.float32)
+
+
+@pytest.mark.parametrize("N,E,k,cap", [(5000, 64, 8, None), (3000, 256, 8, 70), (1000, 896, 16, None), (1, 8, 2, None)],
+                         ids=["E64", "E256-capacity", "E896", "N1"])
+def test_permute_update_bias_matches_separate_calls(N, E, k, cap):
+    """moe_permute_update_bias (the +-gamma step made inside the permute's launches) gives the
+    same counts, offsets, permutation and rows as moe_permute(_capacity), and the same bias and
+    max/mean as moe_bias_update after it, bit for bit; the oracle's bias step agrees."""
+    rng = np.random.default_rng(N + E)
+    idx = torch.from_numpy(np.stack([rng.choice(E, k, replace=False) for _ in range(N)]).astype(np.int32)).cuda()
+    xn = torch.randn(N, 128, device="cuda").to(torch.bfloat16)
+    b0 = torch.from_numpy(rng.standard_normal(E).astype(np.float32) * 0.01).cuda()
+    ref = moe.moe_permute(xn, idx, E, capacity=cap)
+    b_ref, mom_ref = b0.clone(), torch.empty(1, device="cuda")
+    moe.moe_bias_update(ref[0], b_ref, N * k, 1e-3, mom_ref)
+    b_got, mom_got = b0.clone(), torch.empty(1, device="cuda")
+    got = moe.moe_permute(xn, idx, E, capacity=cap, bias_step=(1e-3, b_got, mom_got))
+    torch.cuda.synchronize()
+    assert moe.last_device_status() == 0
+    kept = int(ref[1][-1])  # rows past offsets[E] (dropped slots' room) are not written
+    for name, a, b in zip(("counts", "offsets", "row_map", "perm_token", "x_perm"), got, ref):
+        if name in ("perm_token", "x_perm"):
+            a, b = a[:kept], b[:kept]
+        assert torch.equal(a, b), name
+    assert torch.equal(b_got, b_ref) and torch.equal(mom_got, mom_ref)
+    want, mm = moe_oracle.bias_update(b0.cpu().numpy(), ref[0].cpu().numpy(), N * k, 1e-3)
+    assert np.array_equal(b_got.cpu().numpy(), want) and abs(mom_got.item() - mm) <= 1e-6 * mm

@@ -110,6 +110,7 @@ def test_special_scores_order():
     _, idx, _, _ = moe.moe_router_topk(x.cuda(), w.cuda(), None, k)
     torch.cuda.synchronize()
     assert idx[0].cpu().tolist() == expect
+    assert moe.last_device_status() == -5  # NaN and -inf logits: reported, routed by the order rule
     # tensor-core path with finite weights only (the split needs finite weights)
     wf = w.clone()
     wf[3, 0], wf[4, 0], wf[9, 0] = -3.0, -3.0, -5.0
@@ -117,6 +118,7 @@ def test_special_scores_order():
     _, idx, _, _ = moe.moe_router_topk_split(x.cuda(), moe.moe_router_split(wf.cuda()), None, 8)
     torch.cuda.synchronize()
     assert idx[0].cpu().tolist() == r["idx"][0].tolist()
+    assert moe.last_device_status() == 0
 
 
 @pytest.mark.parametrize("N,D,E,k,fn", [(4096, 1024, 896, 16, "sigmoid"), (8192, 2048, 64, 8, "sqrt_softplus"),
