@@ -122,7 +122,12 @@ def algorithmic(cfg, k=None, copy_rows=False):
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+    """nvidia-smi samples (every 20 ms) of SM clock, power and throttle reasons; summary()
+    keeps the samples whose timestamps fall inside a host-time window (the timed region)."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index):
         self.gpu = gpu_index
@@ -132,12 +137,9 @@ class ClockSampler:
     def __enter__(self):
         fd, self.path = tempfile.mkstemp(suffix=".csv")
         os.close(fd)
-        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits", "-lms", "100",
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "20",
                  "-i", str(self.gpu)], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except (FileNotFoundError, OSError):
             self.proc = None
@@ -152,29 +154,49 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
-    def summary(self):
-        if self.proc is None or not os.path.exists(self.path):
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        sm, smax, reasons = [], [], set()
+    def _rows(self):
+        if getattr(self, "_parsed", None) is not None:
+            return self._parsed
+        import datetime
+        rows = []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as f:
             for line in f:
                 p = [x.strip() for x in line.split(",")]
-                if len(p) < 9:
+                if len(p) < 10:
                     continue
                 try:
-                    sm.append(float(p[1]))
-                    smax.append(float(p[2]))
+                    ts = datetime.datetime.strptime(p[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    sm, smax = float(p[2]), float(p[3])
                 except ValueError:
                     continue
-                for nm, v in zip(names, p[5:9]):
-                    if v.lower() == "active":
-                        reasons.add(nm)
+                try:
+                    pw = float(p[4])
+                except ValueError:
+                    pw = None
+                act = {nm for nm, v in zip(names, p[6:10]) if v.lower() == "active"}
+                rows.append((ts, sm, smax, pw, act))
         os.unlink(self.path)
-        if not sm:
+        self._parsed = rows
+        return rows
+
+    def summary(self, window=None):
+        if self.proc is None or (getattr(self, "_parsed", None) is None and not os.path.exists(self.path)):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = self._rows()
+        scope = "timed region"
+        if window is not None:
+            inside = [r for r in rows if window[0] <= r[0] <= window[1]]
+            if not inside:  # region shorter than the sampling period: the samples around it
+                inside = sorted(rows, key=lambda r: abs(r[0] - 0.5 * (window[0] + window[1])))[:3]
+                scope = "nearest samples to the timed region"
+            rows = inside
+        if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        pw = [r[3] for r in rows if r[3] is not None]
+        return {"sm_mhz": statistics.median(r[1] for r in rows), "sm_max_mhz": max(r[2] for r in rows),
+                "reasons": sorted(set().union(*[r[4] for r in rows])), "samples": len(rows), "scope": scope,
+                "power_w_median": statistics.median(pw) if pw else None, "power_w_max": max(pw) if pw else None}
 
 
 REJECT_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
@@ -280,43 +302,44 @@ def time_device(wl, steps, warmup, world):
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
+    h0 = time.time()
     ms = _timed(fwd, steps)
+    h1 = time.time()
     if world > 1:
         torch.distributed.barrier()
-    return ms, mode
+    return ms, mode, (h0, h1)
 
 
 def stage_times(wl, steps, world):
     """Per-stage device µs over `steps` steps run back to back, as in the headline, with
-    timing events between the stages.  On one GPU every step is the replay of its own CUDA
-    graph of the layer (events captured as graph nodes, one event set per graph, so the
-    replays need no synchronisation between them).  The event nodes cut the programmatic
-    overlap of the kernels on both sides of each, so the stage sum runs a little above
-    the headline step.  With replicas: eager steps."""
+    timing events between the stages.  On one GPU the steps are one CUDA graph holding all
+    `steps` forwards one after another (every step with its own events, captured as event
+    nodes), replayed once to warm it and once to time it.  The event nodes cut the
+    programmatic overlap of the kernels on both sides of each, so the stage sum runs a
+    little above the headline step.  With replicas: eager steps."""
     evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(7)] for _ in range(steps)]
     if world == 1:
         s = torch.cuda.Stream()
         s.wait_stream(torch.cuda.current_stream())
-        graphs = []
-        for i in range(steps):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=s):
-                wl.run(events=evs[i])
-            graphs.append(g)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for e in evs:
+                wl.run(events=e)
         torch.cuda.current_stream().wait_stream(s)
-        for g in graphs:  # every graph's first replay happens before the timed pass
-            g.replay()
-        steps_fn = [g.replay for g in graphs]
-        how = "back-to-back replays of CUDA graphs of the step with event nodes between the stages"
+        g.replay()  # warm: the graph's first replay happens before the timed one
+        torch.cuda.synchronize()
+        run = g.replay
+        how = "one CUDA graph of the back-to-back steps with event nodes between the stages, second replay"
     else:
-        steps_fn = [(lambda e=e: wl.run(events=e)) for e in evs]
+        run = lambda: [wl.run(events=e) for e in evs]
         how = "eager steps with events between the stages"
     torch.cuda.synchronize()
-    for fn in steps_fn:
-        fn()
+    h0 = time.time()
+    run()
     torch.cuda.synchronize()
+    h1 = time.time()
     acc = {n: [e[j].elapsed_time(e[j + 1]) for e in evs] for j, n in enumerate(Workload.STAGES)}
-    return {n: 1e3 * statistics.mean(v) for n, v in acc.items()}, how
+    return {n: 1e3 * statistics.mean(v) for n, v in acc.items()}, how, (h0, h1)
 
 
 def time_permute_copy(wl, steps):
@@ -452,12 +475,12 @@ def roofline_of(flops, bytes_, us, pk, long_run, dtype):
 def measure(wl, steps, warmup, world, pk, e2e_steps):
     """Every number of one workload: headline graph replays, stage times, roofline, e2e."""
     cfg, k, L = wl.cfg, wl.k, wl.layer
-    total_ms, mode = time_device(wl, steps, warmup, world)
+    total_ms, mode, window = time_device(wl, steps, warmup, world)
     total_ms = max_over_ranks(total_ms, world)
     st = moe.last_device_status()
     if st != 0:
         raise SystemExit(f"device status {moe.STATUS.get(st, st)} after {cfg.name} k={k}")
-    stage_us, how = stage_times(wl, steps, world)
+    stage_us, how, stage_window = stage_times(wl, steps, world)
     ms = total_ms / steps
     alg = algorithmic(cfg, k, copy_rows=not L.gather)
     long_run = total_ms >= 1000.0
@@ -467,6 +490,7 @@ def measure(wl, steps, warmup, world, pk, e2e_steps):
     copy_us = time_permute_copy(wl, steps)
     res = {
         "workload": workload_name(cfg, k), "tokens_per_s": cfg.N * world / (ms * 1e-3), "ms_per_step": ms,
+        "timed_window": window, "stage_window": stage_window,
         "steps": steps, "launch": mode, "gemm1_rows": "gathered from xn" if L.gather else "permuted copy x_perm",
         "stage_us": {n: round(v, 2) for n, v in stage_us.items()},
         "stage_sum_us": round(sum(stage_us.values()), 2), "stage_us_from": how,
@@ -656,14 +680,16 @@ def main():
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         head, total_ms = measure(wl, args.steps, args.warmup, world, pk, args.e2e_steps)
-    clocks = clk.summary()
+    clocks = clk.summary(head.pop("timed_window"))
+    head["clocks_stage_pass"] = clk.summary(head.pop("stage_window"))
     remeasured = clock_problem(clocks)
     # every rank measures again if any rank's record is invalid (the timing has barriers)
     if max_over_ranks(1.0 if remeasured else 0.0, world) > 0:
         remeasured = remeasured or "another rank's clock record"
         with ClockSampler(local) as clk:
             head, total_ms = measure(wl, args.steps, args.warmup, world, pk, args.e2e_steps)
-        clocks = clk.summary()
+        clocks = clk.summary(head.pop("timed_window"))
+        head["clocks_stage_pass"] = clk.summary(head.pop("stage_window"))
 
     g = head["grouped_gemm"]
     gemm_ms = g["us"] * 1e-3
@@ -686,6 +712,7 @@ def main():
         "router": head["router"], "permute": head["permute"], "permute_with_row_copy": head["permute_with_row_copy"],
         "combine": head["combine"],
         "stage_us": head["stage_us"], "stage_sum_us": head["stage_sum_us"], "stage_us_from": head["stage_us_from"],
+        "clocks_stage_pass": head["clocks_stage_pass"],
         "gpu_launches": wl.launches * args.steps,
         "clocks": dict(clocks, remeasured_after=remeasured) if remeasured else clocks,
         "e2e": head["e2e"],
@@ -703,7 +730,10 @@ def main():
             if name == cfg.name and kk == k:
                 continue
             w2 = Workload(c2, kk, dev, rank, world, gather=gather if c2.dtype == "bf16" else None)
-            r2, _ = measure(w2, args.steps, args.warmup, world, pk, args.e2e_steps)
+            with ClockSampler(local) as clk2:
+                r2, _ = measure(w2, args.steps, args.warmup, world, pk, args.e2e_steps)
+            r2["clocks"] = clk2.summary(r2.pop("timed_window"))
+            r2["clocks_stage_pass"] = clk2.summary(r2.pop("stage_window"))
             if rank == 0 and c2.bias_steps > 1:
                 r2["load_balance"] = load_balance_trace(w2, c2.bias_steps)
             per[label] = r2

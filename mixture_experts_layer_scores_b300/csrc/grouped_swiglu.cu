@@ -23,7 +23,7 @@
 // MOE_ERR_TIMEOUT in the status word, lets in-flight copies and MMAs land, frees
 // its TMEM and returns.
 //
-// fp32 path: plain CUDA-core kernels (one thread per output element).
+// fp32 path: tiled CUDA-core kernels (64 x 64 output tiles, fp32 FMA chains in K order).
 #include <algorithm>
 #include <cstdlib>
 #include <cstring>
@@ -889,56 +889,146 @@ moe_status_t launch_pair(const CUtensorMap& a, const CUtensorMap& a_half, const 
 
 namespace simt {
 
-__global__ void swiglu_up_kernel(const float* __restrict__ x, const int32_t* __restrict__ offsets, int G,
-                                 int M, int D, int F, const float* __restrict__ wg,
-                                 const float* __restrict__ wu, float* __restrict__ h) {
-  grid_dep_wait();
-  grid_dep_launch();
-  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= (long long)M * F) return;
-  const int r = (int)(i / F), f = (int)(i % F);
-  int lo = 0, hi = G - 1;  // group of row r: largest g with offsets[g] <= r
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (offsets[mid] <= r) lo = mid; else hi = mid - 1;
+// fp32 grouped SwiGLU on CUDA cores: 64 x 64 output tiles, 256 threads with 4 x 4 outputs
+// each, 32-wide K slices staged in shared memory (k-major, so a thread reads four rows or
+// four columns as one float4).  Every output is one fp32 FMA chain over K in index order
+// (bit-identical to a plain dot-product loop).  Tiles are (group, 64-row block, column
+// block); a CTA finds its group by walking the offsets.
+constexpr int TM = 64, TN = 64, TK = 32, PAD = 4;
+
+struct SimtTile {
+  int g, row0, rows, col0;
+  bool valid;
+};
+
+__device__ __forceinline__ SimtTile simt_tile(int t, const int32_t* __restrict__ offsets, int G, int M, int CB) {
+  SimtTile r{0, 0, 0, 0, false};
+  int base = 0;
+  for (int g = 0; g < G; ++g) {
+    const int s = min(max(offsets[g], 0), M);
+    const int e = min(max(offsets[g + 1], s), M);
+    const int n = ((e - s + TM - 1) / TM) * CB;
+    if (t < base + n) {
+      const int local = t - base;
+      const int rb = local / CB;
+      r.g = g;
+      r.row0 = s + rb * TM;
+      r.rows = min(TM, e - r.row0);
+      r.col0 = (local - rb * CB) * TN;
+      r.valid = true;
+      return r;
+    }
+    base += n;
   }
-  if (r < offsets[lo] || r >= offsets[lo + 1]) return;
-  const float* xr = x + (size_t)r * D;
-  const float* gr = wg + ((size_t)lo * F + f) * D;
-  const float* ur = wu + ((size_t)lo * F + f) * D;
-  float a = 0.f, b = 0.f;
-  for (int d = 0; d < D; d += 4) {
-    const float4 xv = *reinterpret_cast<const float4*>(xr + d);
-    const float4 gv = *reinterpret_cast<const float4*>(gr + d);
-    const float4 uv = *reinterpret_cast<const float4*>(ur + d);
-    a = fmaf(xv.x, gv.x, a); a = fmaf(xv.y, gv.y, a); a = fmaf(xv.z, gv.z, a); a = fmaf(xv.w, gv.w, a);
-    b = fmaf(xv.x, uv.x, b); b = fmaf(xv.y, uv.y, b); b = fmaf(xv.z, uv.z, b); b = fmaf(xv.w, uv.w, b);
-  }
-  h[(size_t)r * F + f] = (a / (1.0f + expf(-a))) * b;
+  return r;
 }
 
-__global__ void swiglu_down_kernel(const float* __restrict__ h, const int32_t* __restrict__ offsets, int G,
-                                   int M, int D, int F, const float* __restrict__ wd, float* __restrict__ y) {
+// rows [row0, row0 + rows) x cols [k0, k0 + TK) of a row-major [*, ld] matrix into dst[k][m]
+// (transposed), zero beyond `rows` rows.
+__device__ __forceinline__ void stage_t(float (*dst)[TM + PAD], const float* __restrict__ src, int ld, int row0,
+                                        int rows, int k0) {
+  for (int i = threadIdx.x; i < TM * TK / 4; i += blockDim.x) {
+    const int m = i / (TK / 4), kq = (i % (TK / 4)) * 4;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (m < rows) v = *reinterpret_cast<const float4*>(src + (size_t)(row0 + m) * ld + k0 + kq);
+    dst[kq + 0][m] = v.x;
+    dst[kq + 1][m] = v.y;
+    dst[kq + 2][m] = v.z;
+    dst[kq + 3][m] = v.w;
+  }
+}
+
+// H[r, f] = SiLU(x_r . W_gate[g, f]) * (x_r . W_up[g, f])
+__global__ void __launch_bounds__(256, 2) swiglu_up_kernel(const float* __restrict__ x, const int32_t* __restrict__ offsets,
+                                                        int G, int M, int D, int F, const float* __restrict__ wg,
+                                                        const float* __restrict__ wu, float* __restrict__ h) {
+  __shared__ __align__(16) float xs[TK][TM + PAD], gs[TK][TN + PAD], us[TK][TN + PAD];
   grid_dep_wait();
   grid_dep_launch();
-  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= (long long)M * D) return;
-  const int r = (int)(i / D), d = (int)(i % D);
-  int lo = 0, hi = G - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (offsets[mid] <= r) lo = mid; else hi = mid - 1;
+  const int CB = (F + TN - 1) / TN;
+  const SimtTile tl = simt_tile(blockIdx.x, offsets, G, M, CB);
+  if (!tl.valid) return;
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const int ncols = min(TN, F - tl.col0);
+  const float* wgg = wg + ((size_t)tl.g * F + tl.col0) * D;
+  const float* wug = wu + ((size_t)tl.g * F + tl.col0) * D;
+  float ag[4][4] = {}, au[4][4] = {};
+  for (int k0 = 0; k0 < D; k0 += TK) {
+    stage_t(xs, x, D, tl.row0, tl.rows, k0);
+    stage_t(gs, wgg, D, 0, ncols, k0);
+    stage_t(us, wug, D, 0, ncols, k0);
+    __syncthreads();
+#pragma unroll 8
+    for (int k = 0; k < TK; ++k) {
+      const float4 a = *reinterpret_cast<const float4*>(&xs[k][ty * 4]);
+      const float4 b = *reinterpret_cast<const float4*>(&gs[k][tx * 4]);
+      const float4 c = *reinterpret_cast<const float4*>(&us[k][tx * 4]);
+      const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w}, cv[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          ag[i][j] = fmaf(av[i], bv[j], ag[i][j]);
+          au[i][j] = fmaf(av[i], cv[j], au[i][j]);
+        }
+    }
+    __syncthreads();
   }
-  if (r < offsets[lo] || r >= offsets[lo + 1]) return;
-  const float* hr = h + (size_t)r * F;
-  const float* wr = wd + ((size_t)lo * D + d) * F;
-  float a = 0.f;
-  for (int f = 0; f < F; f += 4) {
-    const float4 hv = *reinterpret_cast<const float4*>(hr + f);
-    const float4 wv = *reinterpret_cast<const float4*>(wr + f);
-    a = fmaf(hv.x, wv.x, a); a = fmaf(hv.y, wv.y, a); a = fmaf(hv.z, wv.z, a); a = fmaf(hv.w, wv.w, a);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = ty * 4 + i;
+    if (r >= tl.rows) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int c = tx * 4 + j;
+      if (c < ncols) {
+        const float a = ag[i][j];
+        h[(size_t)(tl.row0 + r) * F + tl.col0 + c] = (a / (1.0f + expf(-a))) * au[i][j];
+      }
+    }
   }
-  y[(size_t)r * D + d] = a;
+}
+
+// Y[r, d] = H_r . W_down[g, d]
+__global__ void __launch_bounds__(256, 2) swiglu_down_kernel(const float* __restrict__ h, const int32_t* __restrict__ offsets,
+                                                          int G, int M, int D, int F, const float* __restrict__ wd,
+                                                          float* __restrict__ y) {
+  __shared__ __align__(16) float hs[TK][TM + PAD], ds[TK][TN + PAD];
+  grid_dep_wait();
+  grid_dep_launch();
+  const int CB = (D + TN - 1) / TN;
+  const SimtTile tl = simt_tile(blockIdx.x, offsets, G, M, CB);
+  if (!tl.valid) return;
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const int ncols = min(TN, D - tl.col0);
+  const float* wdg = wd + ((size_t)tl.g * D + tl.col0) * F;
+  float acc[4][4] = {};
+  for (int k0 = 0; k0 < F; k0 += TK) {
+    stage_t(hs, h, F, tl.row0, tl.rows, k0);
+    stage_t(ds, wdg, F, 0, ncols, k0);
+    __syncthreads();
+#pragma unroll 8
+    for (int k = 0; k < TK; ++k) {
+      const float4 a = *reinterpret_cast<const float4*>(&hs[k][ty * 4]);
+      const float4 b = *reinterpret_cast<const float4*>(&ds[k][tx * 4]);
+      const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = ty * 4 + i;
+    if (r >= tl.rows) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int c = tx * 4 + j;
+      if (c < ncols) y[(size_t)(tl.row0 + r) * D + tl.col0 + c] = acc[i][j];
+    }
+  }
 }
 
 }  // namespace simt
@@ -976,14 +1066,16 @@ extern "C" moe_status_t moe_grouped_swiglu(const void* x_perm, moe_dtype_t dtype
     return MOE_ERR_INVALID_ARG;
   cudaStream_t s = as_cuda(stream);
   if (dtype == MOE_F32) {
-    const int T = 256;
-    const long long n1 = (long long)M_total * F, n2 = (long long)M_total * D;
+    // at most (row blocks of M_total + one partial block per group) x column blocks tiles
+    const long long rb = (M_total + simt::TM - 1) / simt::TM + G;
+    const long long t1 = rb * ((F + simt::TN - 1) / simt::TN), t2 = rb * ((D + simt::TN - 1) / simt::TN);
+    if (t1 >= (1LL << 31) || t2 >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
     const moe_status_t st = launch_kernel(
-        simt::swiglu_up_kernel, dim3((unsigned)((n1 + T - 1) / T)), dim3(T), 0, s, static_cast<const float*>(x_perm),
-        offsets, G, M_total, D, F, static_cast<const float*>(w_gate), static_cast<const float*>(w_up),
+        simt::swiglu_up_kernel, dim3((unsigned)t1), dim3(256), 0, s, static_cast<const float*>(x_perm), offsets, G,
+        M_total, D, F, static_cast<const float*>(w_gate), static_cast<const float*>(w_up),
         static_cast<float*>(h_workspace));
     if (st != MOE_OK) return st;
-    return launch_kernel(simt::swiglu_down_kernel, dim3((unsigned)((n2 + T - 1) / T)), dim3(T), 0, s,
+    return launch_kernel(simt::swiglu_down_kernel, dim3((unsigned)t2), dim3(256), 0, s,
                          static_cast<const float*>(h_workspace), offsets, G, M_total, D, F,
                          static_cast<const float*>(w_down), static_cast<float*>(y_perm));
   }

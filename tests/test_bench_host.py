@@ -93,3 +93,28 @@ def test_clock_records_that_invalidate_a_number():
     assert "sw_thermal_slowdown" in bench.clock_problem(dict(ok, reasons=["sw_thermal_slowdown"]))
     assert "no reason" in bench.clock_problem({"sm_mhz": 900.0, "sm_max_mhz": 2032.0, "reasons": []})
     assert bench.clock_problem({"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}) is None
+
+
+def test_clock_summary_keeps_the_timed_window(tmp_path):
+    """nvidia-smi rows are parsed and only those inside the timed region's host-time window
+    are summarised (or the nearest few when the region is shorter than the sampling period)."""
+    import datetime
+    rows = []
+    t0 = datetime.datetime(2026, 12, 3, 6, 0, 0)
+    for i, (mhz, pw, cap) in enumerate([(2032, 300, "Not Active"), (1500, 1090, "Active"), (1400, 1100, "Active"),
+                                        (2032, 250, "Not Active")]):
+        ts = (t0 + datetime.timedelta(milliseconds=100 * i)).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+        rows.append(f"{ts}, 0, {mhz}, 2032, {pw}, 0x0, Not Active, Not Active, Not Active, {cap}")
+    s = bench.ClockSampler(0)
+    s.proc = object()
+    s.path = str(tmp_path / "clk.csv")
+    with open(s.path, "w") as f:
+        f.write("\n".join(rows) + "\n")
+    w0 = t0.timestamp()
+    d = s.summary((w0 + 0.05, w0 + 0.25))
+    assert d["samples"] == 2 and d["sm_mhz"] == 1450 and d["reasons"] == ["sw_power_cap"]
+    assert d["power_w_max"] == 1100 and d["scope"] == "timed region"
+    with open(s.path, "w") as f:
+        f.write("\n".join(rows) + "\n")
+    d = s.summary((w0 + 0.101, w0 + 0.102))
+    assert d["scope"].startswith("nearest") and d["samples"] == 3
