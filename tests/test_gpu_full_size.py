@@ -5,8 +5,11 @@ The oracle checks, at each configuration's real size:
 * counts, offsets, row map and token permutation, bit for bit;
 * the permuted rows, bit for bit, and the expert outputs of the row-gathering GEMM against
   those of the GEMM over the permuted copy, bit for bit;
-* the expert outputs and the layer output of a seeded sample of tokens, computed one expert
-  at a time on the CPU from regenerated weights (bf16 tolerance of tests/parity.py);
+* the expert outputs and the layer output of a seeded sample of tokens that together visit
+  every expert (so every expert's GEMM tiles are checked somewhere), computed one expert at a
+  time on the CPU from regenerated weights (bf16 tolerance of tests/parity.py), and, where
+  the weights fit comfortably in host memory, the same layer outputs through the oracle's
+  token_outputs;
 * the bias step, bit for bit;
 and one property that holds at any size checks the combine over every token:
 out = h + shared + sum_j gate * Y[row_map], evaluated in float64 from the kernel's inputs.
@@ -99,15 +102,16 @@ def test_full_size_layer(name, k):
     assert bool((err <= half_ulp * 1.0001 + 1e-6).all()), float((err - half_ulp).max())
 
     # --- expert outputs and layer output of sampled tokens ----------------------------
-    rng = np.random.default_rng(cfg.seed)
-    tokens = rng.choice(np.where(same)[0], SAMPLE, replace=False)
+    tokens = _covering_sample(r["idx"], np.where(same)[0], cfg.E, cfg.seed)
+    assert set(r["idx"][tokens].ravel().tolist()) == set(r["idx"][same].ravel().tolist())  # every routed expert
     x_s = P.np64(xc[tokens])
     want_y = {}                            # (token position, slot) -> oracle expert output
     for e in sorted({int(v) for v in r["idx"][tokens].ravel()}):
         wg, wu, wd = (P.np64(t) for t in synth.make_expert(cfg, e, "cpu"))
-        for i, t in enumerate(tokens):
-            for j in np.where(r["idx"][t] == e)[0]:
-                want_y[(i, j)] = moe_oracle.swiglu_expert(x_s[i:i + 1], wg, wu, wd)[0]
+        pairs = [(i, j) for i, t in enumerate(tokens) for j in np.where(r["idx"][t] == e)[0]]
+        ys = moe_oracle.swiglu_expert(x_s[[i for i, _ in pairs]], wg, wu, wd)  # one call per expert
+        for (i, j), y in zip(pairs, ys):
+            want_y[(i, j)] = y
     y_gpu = layer.y_perm.cpu()
     got_rows, want_rows = [], []
     for (i, j), y in want_y.items():
@@ -124,6 +128,31 @@ def test_full_size_layer(name, k):
         want_out[i] += r["gate"][tokens[i], j] * y
     P.assert_close("out (sampled)", P.np64(out.cpu()[tokens]), want_out)
     P.delta_close("out - h (sampled)", P.np64(out.cpu()[tokens]), want_out, P.np64(hc[tokens]))
+    if 3 * cfg.E * cfg.D * cfg.F * 2 <= 2e9:  # the oracle's per-token formula, weights cached per expert
+        sh = None
+        if cfg.shared:
+            sh = tuple(P.np64(t) for t in synth.make_expert(cfg, 0, "cpu", shared=True))
+        via = moe_oracle.token_outputs(tokens, x_s, P.np64(hc[tokens]), r["idx"][tokens], r["gate"][tokens],
+                                       lambda e: tuple(t.float().numpy() for t in synth.make_expert(cfg, e, "cpu")),
+                                       sh)
+        P.assert_close("out (sampled, token_outputs)", P.np64(out.cpu()[tokens]), via)
+
+
+def _covering_sample(idx, candidates, E, seed, at_least=SAMPLE):
+    """Seeded tokens, drawn in random order, kept while they visit an expert no kept token
+    visits yet, until every expert is visited (or the candidates run out); at least
+    `at_least` tokens."""
+    rng = np.random.default_rng(seed)
+    order = rng.permutation(candidates)
+    seen, kept = set(), []
+    for t in order:
+        new = set(idx[t].tolist()) - seen
+        if new or len(kept) < at_least:
+            kept.append(int(t))
+            seen |= set(idx[t].tolist())
+        if len(seen) == E and len(kept) >= at_least:
+            break
+    return np.array(kept)
 
 
 def test_generator_bits_equal_on_gpu_and_cpu():
