@@ -236,7 +236,7 @@ class Workload:
     # "bias": the separate bias step of replicas (empty on one GPU, where the permute does it)
     STAGES = ("router", "permute", "grouped_swiglu", "shared", "combine", "bias")
 
-    def __init__(self, cfg, k, dev, rank=0, world=1, gather=None):
+    def __init__(self, cfg, k, dev, rank=0, world=1, gather=None, fuse_shared=True):
         self.cfg, self.k, self.dev, self.world = cfg, k, dev, world
         self.xn, self.h = synth.make_tokens(cfg, dev, seed=cfg.seed + 1000 * rank)
         w_r, b = synth.make_router(cfg, dev)
@@ -244,7 +244,7 @@ class Workload:
         sh = synth.make_shared(cfg, dev)
         dt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
         self.layer = moe.MoELayer(moe.LayerWeights(w_r, b, wg, wu, wd, sh), cfg.N, k, cfg.score_fn,
-                                  cfg.gamma, dtype=dt, gather=gather)
+                                  cfg.gamma, dtype=dt, gather=gather, fuse_shared=fuse_shared)
 
     def run(self, xn=None, h=None, events=None, out=None):
         L = self.layer
@@ -484,7 +484,19 @@ def measure(wl, steps, warmup, world, pk, e2e_steps):
     ms = total_ms / steps
     alg = algorithmic(cfg, k, copy_rows=not L.gather)
     long_run = total_ms >= 1000.0
+    def bound_s(flops, bytes_):  # the roofline time of one phase: the slower of its two bounds
+        pt = pk["bf16_tflops_sustained"] if long_run else pk["bf16_tflops"]
+        return max(flops / (pt * 1e12), bytes_ / (pk["hbm_gbs"] * 1e9))
+    t_phases = bound_s(alg["gemm_flops"], alg["gemm_bytes"])
+    if L.fuse_shared:  # the shared expert's tiles run in the routed experts' launches, after theirs
+        t_phases += bound_s(alg["shared_flops"], alg["shared_bytes"])
+        alg["gemm_flops"] += alg["shared_flops"]
+        alg["gemm_bytes"] += alg["shared_bytes"]
     gemm = roofline_of(alg["gemm_flops"], alg["gemm_bytes"], stage_us["grouped_swiglu"], pk, long_run, cfg.dtype)
+    if L.fuse_shared and cfg.dtype == "bf16":
+        gemm["bound_time_frac"] = t_phases / (stage_us["grouped_swiglu"] * 1e-6)
+        gemm["bound_time_note"] = ("(routed experts' roofline time + shared expert's roofline time) / measured time: "
+                                   "the shared tiles follow the routed ones in each launch")
     gbs = lambda b, us: b / (us * 1e-6) / 1e9
     hbm = pk["hbm_gbs"]
     copy_us = time_permute_copy(wl, steps)
@@ -494,7 +506,8 @@ def measure(wl, steps, warmup, world, pk, e2e_steps):
         "steps": steps, "launch": mode, "gemm1_rows": "gathered from xn" if L.gather else "permuted copy x_perm",
         "stage_us": {n: round(v, 2) for n, v in stage_us.items()},
         "stage_sum_us": round(sum(stage_us.values()), 2), "stage_us_from": how,
-        "grouped_gemm": dict(gemm, kernel="moe_grouped_swiglu_gather" if L.gather else "moe_grouped_swiglu",
+        "grouped_gemm": dict(gemm, kernel="moe_grouped_swiglu_shared (routed + shared expert)" if L.fuse_shared
+                             else ("moe_grouped_swiglu_gather" if L.gather else "moe_grouped_swiglu"),
                              launches="GEMM1+SwiGLU and GEMM2", us=round(stage_us["grouped_swiglu"], 2),
                              tflops=alg["gemm_flops"] / (stage_us["grouped_swiglu"] * 1e-6) / 1e12,
                              algorithmic_gflop=alg["gemm_flops"] / 1e9,
@@ -514,7 +527,7 @@ def measure(wl, steps, warmup, world, pk, e2e_steps):
                     "algorithmic_mb": alg["combine_bytes"] / 1e6},
         "gpu_launches_per_step": wl.launches,
     }
-    if cfg.shared:
+    if cfg.shared and not L.fuse_shared:
         res["shared_expert"] = roofline_of(alg["shared_flops"], alg["shared_bytes"], stage_us["shared"], pk,
                                            long_run, cfg.dtype)
     e2e_ms, bi, bo = time_e2e(wl, e2e_steps, warmup, world)
@@ -654,6 +667,8 @@ def main():
     rows = ap.add_mutually_exclusive_group()
     rows.add_argument("--permute-copy", action="store_true",
                       help="the permute writes the permuted rows x_perm and GEMM1 loads them by TMA")
+    ap.add_argument("--shared-separate", action="store_true",
+                    help="run the shared expert in launches of its own instead of inside the routed experts' launches")
     rows.add_argument("--gather", action="store_true",
                       help="GEMM1 gathers its rows from xn through perm_token (default: the layer "
                            "chooses by size)")
@@ -676,7 +691,7 @@ def main():
     pk, pk_kind = peaks()
     gather = True if args.gather else (False if args.permute_copy else None)
 
-    wl = Workload(cfg, k, dev, rank, world, gather=gather)
+    wl = Workload(cfg, k, dev, rank, world, gather=gather, fuse_shared=not args.shared_separate)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         head, total_ms = measure(wl, args.steps, args.warmup, world, pk, args.e2e_steps)
@@ -693,7 +708,8 @@ def main():
 
     g = head["grouped_gemm"]
     gemm_ms = g["us"] * 1e-3
-    roof = {k2: g[k2] for k2 in ("bound", "achieved", "peak", "unit", "frac", "peak_kind")}
+    roof = {k2: g[k2] for k2 in ("bound", "achieved", "peak", "unit", "frac", "peak_kind", "bound_time_frac",
+                                 "bound_time_note") if k2 in g}
     roof.update({"kernel": f"{g['kernel']} ({g['launches']} launches, one call)",
                  "traffic": recorded_traffic(cfg, wl.layer.gather), "traffic_unit": "bytes per call (ncu)",
                  "peak_source": pk_kind, "timed": head["stage_us_from"],

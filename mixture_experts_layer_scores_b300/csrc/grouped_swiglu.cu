@@ -56,6 +56,7 @@ inline int cta_cap() { return g_max_ctas > 0 ? std::min(g_max_ctas, sm_count()) 
 
 struct Tile {
   int g, row0, rows, nb, mb;
+  int x;  // 1: a tile of the extra group (the shared expert run in the same launch)
 };
 
 template <int ROWS>
@@ -68,6 +69,7 @@ __device__ __forceinline__ Tile decode_rows(int tile, const int* tile_start, int
   }
   Tile t;
   t.g = lo;
+  t.x = 0;
   const int s = min(max(__ldg(offsets + lo), 0), M_total);
   const int e = min(max(__ldg(offsets + lo + 1), s), M_total);
   const int mblk = (e - s + ROWS - 1) / ROWS;
@@ -83,6 +85,32 @@ __device__ __forceinline__ Tile decode_rows(int tile, const int* tile_start, int
 __device__ __forceinline__ Tile decode(int tile, const int* tile_start, int G, const int32_t* offsets,
                                        int M_total, int NB) {
   return decode_rows<BM>(tile, tile_start, G, offsets, M_total, NB);
+}
+
+// The tile list of a launch that also runs an extra group (the shared expert: rows [0, M2) of
+// its own operands): the `routed` tiles of the groups, then NX = ceil(M2/128) * NB extra tiles,
+// which fill the routed tiles' last wave.  (Spreading the extra tiles evenly among the routed
+// ones, with the routed weights marked evict-first and the shared operands evict-last in L2,
+// measured 16 % slower on the DeepSeek-V3 layer: the streamed weights still pushed the shared
+// operands out of L2.)
+struct ExtraList {
+  int routed, NX, M2;
+  __device__ __forceinline__ int total() const { return routed + NX; }
+};
+
+__device__ __forceinline__ Tile decode_list(int t, const ExtraList& L, const int* tile_start, int G,
+                                            const int32_t* offsets, int M_total, int NB) {
+  if (t < L.routed) return decode(t, tile_start, G, offsets, M_total, NB);
+  const int xi = t - L.routed;
+  Tile r;
+  const int mblk = (L.M2 + BM - 1) / BM;
+  r.g = 0;
+  r.x = 1;
+  r.nb = xi / mblk;
+  r.mb = xi - r.nb * mblk;
+  r.row0 = r.mb * BM;
+  r.rows = min(BM, L.M2 - r.row0);
+  return r;
 }
 
 // MODE 0: GEMM1 with SwiGLU epilogue (B = gate rows ; up rows, 128 output columns per tile)
@@ -110,7 +138,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
                     const __grid_constant__ CUtensorMap map_b1, const __grid_constant__ CUtensorMap map_out,
                     const int32_t* __restrict__ offsets, int G, int M_total, int K, int NOUT,
                     __nv_bfloat16* __restrict__ out, const __nv_bfloat16* __restrict__ xg, int NX,
-                    const int32_t* __restrict__ perm, int b_planes, int nbuf, int* __restrict__ status) {
+                    const int32_t* __restrict__ perm, int b_planes, int nbuf, int* __restrict__ status,
+                    const __grid_constant__ CUtensorMap map_a2, const __grid_constant__ CUtensorMap map_b2,
+                    const __grid_constant__ CUtensorMap map_out2, int M2, __nv_bfloat16* __restrict__ out2,
+                    int b2_planes) {
   constexpr bool SWIGLU = MODE != 1;
   constexpr int TN = SWIGLU ? BN / 2 : BN;  // output columns per tile
   constexpr int NTHR = kThreads<MODE>;
@@ -199,7 +230,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
-  const int total_tiles = tile_start[G];
+  ExtraList XL;
+  XL.routed = tile_start[G];
+  XL.M2 = MODE != 2 ? M2 : 0;
+  XL.NX = XL.M2 > 0 ? ((XL.M2 + BM - 1) / BM) * NB : 0;
+  const int total_tiles = XL.total();
+  auto tile_at = [&](int tile) { return decode_list(tile, XL, tile_start, G, offsets, M_total, NB); };
 
   if (warp == 0) {
     if (lane == 0) {
@@ -207,21 +243,23 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
       int stage = 0;
       uint32_t phase = 0, issued = 0, issued_par = 0;
       for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
-        const Tile tl = decode(tile, tile_start, G, offsets, M_total, NB);
-        const int brow = tl.g * NOUT + tl.nb * TN;
+        const Tile tl = tile_at(tile);
+        const int brow = (tl.x ? 0 : tl.g * NOUT) + tl.nb * TN;
+        const CUtensorMap* mb = tl.x ? &map_b2 : &map_b0;
+        const int planes = tl.x ? b2_planes : b_planes;
         bool ok = true;
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, status, true)) { ok = false; break; }
           const uint32_t a_dst = smem_u32(smem + stage * STAGE_BYTES);
           const uint32_t b_dst = a_dst + A_BYTES;
           mbar_expect_tx(full_bar(stage), B_BYTES);
-          if (SWIGLU && b_planes != 0) {  // gate and up rows as the two planes of one box
-            tma_load_3d(b_dst, &map_b0, kb * BK, brow, 0, full_bar(stage));
+          if (SWIGLU && planes != 0) {  // gate and up rows as the two planes of one box
+            tma_load_3d(b_dst, mb, kb * BK, brow, 0, full_bar(stage));
           } else if (SWIGLU) {
             tma_load_2d(b_dst, &map_b0, kb * BK, brow, full_bar(stage));
             tma_load_2d(b_dst + B_BYTES / 2, &map_b1, kb * BK, brow, full_bar(stage));
           } else {
-            tma_load_2d(b_dst, &map_b0, kb * BK, brow, full_bar(stage));
+            tma_load_2d(b_dst, mb, kb * BK, brow, full_bar(stage));
           }
           issued |= 1u << stage;
           issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
@@ -269,12 +307,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
       int stage = 0;
       uint32_t phase = 0, issued = 0, issued_par = 0;
       for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
-        const Tile tl = decode(tile, tile_start, G, offsets, M_total, NB);
+        const Tile tl = tile_at(tile);
+        const CUtensorMap* ma = tl.x ? &map_a2 : &map_a;
         bool ok = true;
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, status, true)) { ok = false; break; }
           mbar_expect_tx(full_bar(stage), A_BYTES);
-          tma_load_2d(smem_u32(smem + stage * STAGE_BYTES), &map_a, kb * BK, tl.row0, full_bar(stage));
+          tma_load_2d(smem_u32(smem + stage * STAGE_BYTES), ma, kb * BK, tl.row0, full_bar(stage));
           issued |= 1u << stage;
           issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -307,7 +346,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
     };
     const int kb_decode = KB > 2 ? 1 : 0, kb_tokens = KB > 2 ? 2 : KB - 1;
     if (blockIdx.x < total_tiles) {
-      tl_next = decode(blockIdx.x, tile_start, G, offsets, M_total, NB);
+      tl_next = tile_at(blockIdx.x);
       load_tokens();
     }
     for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
@@ -342,7 +381,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
         }
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         if (more) {
-          if (kb == kb_decode) tl_next = decode(tile + gridDim.x, tile_start, G, offsets, M_total, NB);
+          if (kb == kb_decode) tl_next = tile_at(tile + gridDim.x);
           if (kb == kb_tokens) load_tokens();
         }
       }
@@ -361,11 +400,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row_local = q * 32 + lane;
     const uint32_t my_staging = smem_u32(staging) + (uint32_t)(q * nbuf * STAGING_BYTES);
-    const uint32_t gcol = b_planes == 2 ? TN : 0;  // up rows came first in B
     int acc = 0, bi = 0, stores = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
-      const Tile tl = decode(tile, tile_start, G, offsets, M_total, NB);
+      const Tile tl = tile_at(tile);
+      const uint32_t gcol = (tl.x ? b2_planes : b_planes) == 2 ? TN : 0;  // up rows came first in B
+      const CUtensorMap* mo = tl.x ? &map_out2 : &map_out;
+      __nv_bfloat16* optr = tl.x ? out2 : out;
       const bool ok = mbar_wait(tfull_bar(acc), acc_phase, abort_flag, status, true);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
@@ -420,13 +461,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_2d(&map_out, tl.nb * TN + ocol, tl.row0 + q * 32, buf);
+            tma_store_2d(mo, tl.nb * TN + ocol, tl.row0 + q * 32, buf);
             bulk_commit();
           }
           ++stores;
           if (++bi == nbuf) bi = 0;
         } else if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(out + (size_t)(tl.row0 + row_local) * NOUT + tl.nb * TN + ocol);
+          uint4* dst = reinterpret_cast<uint4*>(optr + (size_t)(tl.row0 + row_local) * NOUT + tl.nb * TN + ocol);
 #pragma unroll
           for (int c = 0; c < 8; ++c) dst[c] = packed[c];
         }
@@ -844,11 +885,22 @@ size_t smem_bytes(int G, int nbuf) {
   return 1024 + (size_t)STAGES * STAGE_BYTES + (size_t)4 * nbuf * STAGING_BYTES + 256 + (size_t)(G + 32) * 4;
 }
 
+// The extra group of a launch (the shared expert's tiles in the routed experts' launch): its
+// A rows, B weights (b_planes as for the routed B) and output, M rows; M = 0: none.
+struct ExtraGroup {
+  const CUtensorMap* a = nullptr;
+  const CUtensorMap* b = nullptr;
+  const CUtensorMap* out_map = nullptr;
+  int M = 0;
+  void* out = nullptr;
+  int b_planes = 0;
+};
+
 template <int MODE>
 moe_status_t launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1, const CUtensorMap& out_map,
                     const int32_t* offsets, int G, int M_total, int K, int NOUT, void* out, int* status,
                     cudaStream_t s, const void* xg = nullptr, int NX = 0, const int32_t* perm = nullptr,
-                    int b_planes = 0) {
+                    int b_planes = 0, const ExtraGroup& x = ExtraGroup()) {
   const int nbuf = smem_bytes(G, 2) <= 227 * 1024 ? 2 : 1;  // double-buffer the staging if it fits
   const size_t smem = smem_bytes(G, nbuf);
   auto kern = grouped_gemm_kernel<MODE>;
@@ -856,11 +908,13 @@ moe_status_t launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorM
     return MOE_ERR_CUDA;
   const int TN = MODE != 1 ? BN / 2 : BN;
   const long long NB = (NOUT + TN - 1) / TN;
-  const long long max_tiles = ((long long)(M_total + BM - 1) / BM + G) * NB;
+  const int M2 = MODE != 2 ? x.M : 0;
+  const long long max_tiles = ((long long)(M_total + BM - 1) / BM + G) * NB + ((long long)(M2 + BM - 1) / BM) * NB;
   const int grid = (int)std::min<long long>(max_tiles, (long long)cta_cap());
   return launch_kernel(kern, dim3(grid), dim3(kThreads<MODE>), smem, s, a, b0, b1, out_map, offsets, G, M_total, K,
                        NOUT, static_cast<__nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(xg), NX, perm,
-                       b_planes, nbuf, status);
+                       b_planes, nbuf, status, M2 > 0 ? *x.a : a, M2 > 0 ? *x.b : b0, M2 > 0 ? *x.out_map : out_map,
+                       M2, static_cast<__nv_bfloat16*>(M2 > 0 ? x.out : out), x.b_planes);
 }
 
 size_t pair_smem_bytes(int G, int nbuf) {
@@ -1134,6 +1188,77 @@ extern "C" moe_status_t moe_grouped_swiglu_ex(const void* x_perm, moe_dtype_t dt
                                              h_workspace, y_perm, stream);
   moe::tc::g_max_ctas = saved;
   return st;
+}
+
+extern "C" moe_status_t moe_grouped_swiglu_shared(const void* x_perm, const int32_t* offsets, int G, int M_total,
+                                                  int D, int F, const void* w_gate, const void* w_up,
+                                                  const void* w_down, void* h_workspace, void* y_perm,
+                                                  const void* xn, int N, const void* ws_gate, const void* ws_up,
+                                                  const void* ws_down, void* hs_workspace, void* shared_y,
+                                                  moe_stream_t stream) {
+  using namespace moe;
+  if (G < 1 || M_total < 0 || D <= 0 || F <= 0 || N < 0) return MOE_ERR_INVALID_ARG;
+  if (D % 64 != 0 || F % 64 != 0 || G > tc::MAX_GROUPS) return MOE_ERR_UNSUPPORTED;
+  if ((long long)G * F >= (1LL << 31) || (long long)G * D >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
+  if (M_total > 0 && (!x_perm || !offsets || !w_gate || !w_up || !w_down || !h_workspace || !y_perm))
+    return MOE_ERR_INVALID_ARG;
+  if (N > 0 && (!xn || !ws_gate || !ws_up || !ws_down || !hs_workspace || !shared_y)) return MOE_ERR_INVALID_ARG;
+  for (const void* p : {x_perm, (const void*)w_gate, w_up, w_down, (const void*)h_workspace, (const void*)y_perm, xn,
+                        ws_gate, ws_up, ws_down, (const void*)hs_workspace, (const void*)shared_y})
+    if (p && !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  if (N == 0)
+    return moe_grouped_swiglu(x_perm, MOE_BF16, offsets, G, M_total, D, F, w_gate, w_up, w_down, h_workspace, y_perm,
+                              stream);
+  if (!offsets) return MOE_ERR_INVALID_ARG;
+  // Routed experts large enough for CTA pairs run on the pair kernels first; the shared
+  // expert then runs alone as the extra group of one-CTA launches with no routed rows.
+  const bool separate = M_total == 0 || tc::use_pair(G, M_total);
+  if (separate && M_total > 0) {
+    const moe_status_t st = moe_grouped_swiglu(x_perm, MOE_BF16, offsets, G, M_total, D, F, w_gate, w_up, w_down,
+                                               h_workspace, y_perm, stream);
+    if (st != MOE_OK) return st;
+  }
+  const int Mr = separate ? 0 : M_total;  // routed rows in these launches
+  int* status = device_status_word();
+  if (!status) return MOE_ERR_CUDA;
+  cudaStream_t s = as_cuda(stream);
+  CUtensorMap ma, mg, mu, mh, md, mho, myo, mgu;
+  CUtensorMap xa, xgu, xh, xd, xho, xyo;
+  int planes = 0, xplanes = 0;
+  if (!tc::make_map_bf16(&xa, xn, (uint64_t)N, (uint64_t)D, tc::BM) ||
+      !tc::make_map_bf16(&xh, hs_workspace, (uint64_t)N, (uint64_t)F, tc::BM) ||
+      !tc::make_map_bf16(&xd, ws_down, (uint64_t)D, (uint64_t)F, tc::BN) ||
+      !tc::make_map_bf16(&xho, hs_workspace, (uint64_t)N, (uint64_t)F, 32) ||
+      !tc::make_map_bf16(&xyo, shared_y, (uint64_t)N, (uint64_t)D, 32))
+    return MOE_ERR_CUDA;
+  if (!tc::make_map_gate_up(&xgu, ws_gate, ws_up, (uint64_t)F, (uint64_t)D, tc::BN / 2, &xplanes))
+    return MOE_ERR_UNSUPPORTED;  // the shared gate/up pair must form one two-plane map
+  bool gu = false;
+  if (Mr > 0) {
+    if (!tc::make_map_bf16(&ma, x_perm, (uint64_t)Mr, (uint64_t)D, tc::BM) ||
+        !tc::make_map_bf16(&mg, w_gate, (uint64_t)G * F, (uint64_t)D, tc::BN / 2) ||
+        !tc::make_map_bf16(&mu, w_up, (uint64_t)G * F, (uint64_t)D, tc::BN / 2) ||
+        !tc::make_map_bf16(&mh, h_workspace, (uint64_t)Mr, (uint64_t)F, tc::BM) ||
+        !tc::make_map_bf16(&md, w_down, (uint64_t)G * D, (uint64_t)F, tc::BN) ||
+        !tc::make_map_bf16(&mho, h_workspace, (uint64_t)Mr, (uint64_t)F, 32) ||
+        !tc::make_map_bf16(&myo, y_perm, (uint64_t)Mr, (uint64_t)D, 32))
+      return MOE_ERR_CUDA;
+    gu = tc::make_map_gate_up(&mgu, w_gate, w_up, (uint64_t)G * F, (uint64_t)D, tc::BN / 2, &planes);
+  } else {  // no routed tiles: the shared expert's maps stand in for the unused routed ones
+    ma = xa; mgu = xgu; mg = xgu; mu = xgu; mh = xh; md = xd; mho = xho; myo = xyo;
+    gu = true;
+    planes = xplanes;
+  }
+  tc::ExtraGroup x1;
+  x1.a = &xa; x1.b = &xgu; x1.out_map = &xho; x1.M = N; x1.out = hs_workspace; x1.b_planes = xplanes;
+  moe_status_t st = gu ? tc::launch<0>(ma, mgu, mgu, mho, offsets, G, Mr, D, F, h_workspace, status, s, nullptr, 0,
+                                       nullptr, planes, x1)
+                       : tc::launch<0>(ma, mg, mu, mho, offsets, G, Mr, D, F, h_workspace, status, s, nullptr, 0,
+                                       nullptr, 0, x1);
+  if (st != MOE_OK) return st;
+  tc::ExtraGroup x2;
+  x2.a = &xh; x2.b = &xd; x2.out_map = &xyo; x2.M = N; x2.out = shared_y; x2.b_planes = 0;
+  return tc::launch<1>(mh, md, md, myo, offsets, G, Mr, F, D, y_perm, status, s, nullptr, 0, nullptr, 0, x2);
 }
 
 extern "C" moe_status_t moe_grouped_swiglu_gather(const void* xn, int N, const int32_t* perm_token,

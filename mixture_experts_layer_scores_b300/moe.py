@@ -26,7 +26,7 @@ EXPORTS = ("moe_status_string", "moe_last_device_status", "moe_version", "moe_ro
            "moe_permute_noalloc_max_scratch_bytes", "moe_router_split_bytes", "moe_router_split",
            "moe_router_topk_split", "moe_router_topk_split_workspace_bytes", "moe_permute_capacity",
            "moe_grouped_swiglu_gather", "moe_grouped_swiglu_ex", "moe_expert_capacity",
-           "moe_selftest_bounded_wait", "moe_permute_update_bias")
+           "moe_selftest_bounded_wait", "moe_permute_update_bias", "moe_grouped_swiglu_shared")
 
 
 class MoEError(RuntimeError):
@@ -71,6 +71,8 @@ def load():
         "moe_selftest_bounded_wait": ([vp, ctypes.c_longlong, vp, vp], i32),
         "moe_permute_update_bias": ([vp, i32, i32, i32, vp, i32, i32, i32, vp, vp, vp, vp, vp, vp, sz, f32, vp,
                                      vp, vp], i32),
+        "moe_grouped_swiglu_shared": ([vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp,
+                                       vp], i32),
     }
     for name, (args, res) in sig.items():
         f = getattr(L, name)
@@ -338,6 +340,41 @@ def moe_grouped_swiglu(x_perm, offsets, w_gate, w_up, w_down, h_workspace=None, 
     return y_perm
 
 
+def moe_grouped_swiglu_shared(x_perm, offsets, w_gate, w_up, w_down, xn, shared, h_workspace=None, y_perm=None,
+                              hs_workspace=None, shared_y=None, stream=None):
+    """The routed experts' SwiGLU and the always-on shared expert's (shared = (w_gate[1,F,D],
+    w_up[1,F,D], w_down[1,D,F]) on xn) in the same two launches (bf16).  Returns (y_perm, shared_y)."""
+    L = load()
+    M, D = x_perm.shape
+    G, F, _ = w_gate.shape
+    N = xn.shape[0]
+    dt, dev = x_perm.dtype, x_perm.device
+    sg, su, sd = shared
+    _need("x_perm", x_perm, torch.bfloat16)
+    _need("offsets", offsets, torch.int32, (G + 1,), dev)
+    _need("w_gate", w_gate, dt, (G, F, D), dev)
+    _need("w_up", w_up, dt, (G, F, D), dev)
+    _need("w_down", w_down, dt, (G, D, F), dev)
+    _need("xn", xn, dt, (N, D), dev)
+    _need("shared w_gate", sg, dt, (1, F, D), dev)
+    _need("shared w_up", su, dt, (1, F, D), dev)
+    _need("shared w_down", sd, dt, (1, D, F), dev)
+    _need("h_workspace", h_workspace, dt, (M, F), dev)
+    _need("y_perm", y_perm, dt, (M, D), dev)
+    _need("hs_workspace", hs_workspace, dt, (N, F), dev)
+    _need("shared_y", shared_y, dt, (N, D), dev)
+    e = lambda *sh: torch.empty(*sh, dtype=dt, device=dev)
+    h_workspace = e(M, F) if h_workspace is None else h_workspace
+    y_perm = e(M, D) if y_perm is None else y_perm
+    hs_workspace = e(N, F) if hs_workspace is None else hs_workspace
+    shared_y = e(N, D) if shared_y is None else shared_y
+    _cuda(x_perm, offsets, w_gate, w_up, w_down, xn, sg, su, sd, h_workspace, y_perm, hs_workspace, shared_y)
+    _chk("moe_grouped_swiglu_shared", L.moe_grouped_swiglu_shared(
+        _p(x_perm), _p(offsets), G, M, D, F, _p(w_gate), _p(w_up), _p(w_down), _p(h_workspace), _p(y_perm),
+        _p(xn), N, _p(sg), _p(su), _p(sd), _p(hs_workspace), _p(shared_y), _stream(stream)))
+    return y_perm, shared_y
+
+
 def moe_grouped_swiglu_gather(xn, perm_token, offsets, w_gate, w_up, w_down, h_workspace=None,
                               y_perm=None, stream=None):
     """Grouped SwiGLU whose row i reads xn[perm_token[i]] directly (bf16).  Returns y_perm."""
@@ -434,7 +471,7 @@ class MoELayer:
     """Top-k MoE FFN layer forward on one GPU, with reusable device buffers."""
 
     def __init__(self, weights: LayerWeights, N: int, k: int, score_fn="softmax", gamma=1e-3,
-                 dtype=torch.bfloat16, capacity_factor=None, gather=None):
+                 dtype=torch.bfloat16, capacity_factor=None, gather=None, fuse_shared=True):
         """gather (bf16): the first expert GEMM reads its rows from xn through perm_token
         instead of from a permuted copy, which is then never written; False writes x_perm in
         the permute and runs the GEMM on it.  None chooses by size: gathering costs the GEMM
@@ -479,6 +516,10 @@ class MoELayer:
             self.sh_y = e(N, self.D, dt=dtype)
         else:
             self.sh_y = None
+        # the shared expert's tiles ride in the routed experts' launches (same d_ff, bf16, the
+        # routed rows read from x_perm)
+        self.fuse_shared = bool(fuse_shared) and w.shared is not None and dtype == torch.bfloat16 \
+            and not self.gather and w.shared[0].shape[1] == self.F
 
     def forward(self, xn, h, update_bias=True, stream=None, out=None):
         """out = h + shared(xn) + sum_j gate_j Expert_j(xn), and the +-gamma bias step on
@@ -521,9 +562,13 @@ class MoELayer:
                     bias_step=(self.gamma, self.w.bias, self.mom) if update_bias else None)
 
     def experts(self, xn, stream=None):
-        """Every routed expert's SwiGLU FFN over its block of permuted rows -> y_perm."""
+        """Every routed expert's SwiGLU FFN over its block of permuted rows -> y_perm (and the
+        shared expert's -> sh_y, in the same launches, when fused)."""
         w = self.w
-        if self.gather:
+        if self.fuse_shared:
+            moe_grouped_swiglu_shared(self.x_perm, self.offsets, w.w_gate, w.w_up, w.w_down, xn, w.shared,
+                                      self.h_ws, self.y_perm, self.sh_h, self.sh_y, stream=stream)
+        elif self.gather:
             moe_grouped_swiglu_gather(xn, self.perm_token, self.offsets, w.w_gate, w.w_up,
                                       w.w_down, self.h_ws, self.y_perm, stream=stream)
         else:
@@ -532,7 +577,7 @@ class MoELayer:
 
     def shared_expert(self, xn, stream=None):
         w = self.w
-        if w.shared is not None:
+        if w.shared is not None and not self.fuse_shared:
             moe_grouped_swiglu(xn, self.sh_offsets, w.shared[0], w.shared[1], w.shared[2],
                                self.sh_h, self.sh_y, stream=stream)
 
@@ -564,4 +609,5 @@ class MoELayer:
         router = 3 if self.tc_router else 1
         permute = 3 + (0 if self.gather else 1)  # histogram, scan (+ bias step), rank (+ row copy)
         bias = 0 if fused_bias else 1
-        return router + permute + 2 + (2 if self.w.shared else 0) + 1 + bias
+        shared = 2 if (self.w.shared is not None and not self.fuse_shared) else 0
+        return router + permute + 2 + shared + 1 + bias

@@ -365,3 +365,30 @@ def test_permute_update_bias_matches_separate_calls(N, E, k, cap):
     assert torch.equal(b_got, b_ref) and torch.equal(mom_got, mom_ref)
     want, mm = moe_oracle.bias_update(b0.cpu().numpy(), ref[0].cpu().numpy(), N * k, 1e-3)
     assert np.array_equal(b_got.cpu().numpy(), want) and abs(mom_got.item() - mm) <= 1e-6 * mm
+
+
+@pytest.mark.parametrize("N,D,E,F,k", [(1000, 256, 32, 128, 4), (300, 512, 16, 256, 2), (2048, 256, 4, 128, 2),
+                                       (4096, 7168, 256, 2048, 8)],
+                         ids=["small", "ragged", "pair-routed-then-shared-alone", "deepseek_v3"])
+def test_shared_expert_in_routed_launches(N, D, E, F, k):
+    """moe_grouped_swiglu_shared (the shared expert's tiles after the routed experts' tiles in
+    the same two launches) gives the same bits as the routed call followed by the shared
+    expert's own call, and the oracle's shared expert within the bf16 tolerance."""
+    cfg = synth.scaled(synth.CONFIGS["deepseek_v3"], N=N, D=D, E=E, F=F, k=k, F_shared=F)
+    xn, _ = synth.make_tokens(cfg, "cuda")
+    wg, wu, wd = synth.make_experts(cfg, "cuda")
+    sh = synth.make_shared(cfg, "cuda")
+    rng = np.random.default_rng(N)
+    idx = torch.from_numpy(np.stack([rng.choice(E, k, replace=False) for _ in range(N)]).astype(np.int32)).cuda()
+    counts, offsets, row_map, perm, x_perm = moe.moe_permute(xn, idx, E)
+    y_ref = moe.moe_grouped_swiglu(x_perm, offsets, wg, wu, wd)
+    off_sh = torch.tensor([0, N], dtype=torch.int32, device="cuda")
+    sh_ref = moe.moe_grouped_swiglu(xn, off_sh, *sh)
+    y, sh_y = moe.moe_grouped_swiglu_shared(x_perm, offsets, wg, wu, wd, xn, sh)
+    torch.cuda.synchronize()
+    assert moe.last_device_status() == 0
+    assert torch.equal(y, y_ref) and torch.equal(sh_y, sh_ref)
+    if N * D <= 1 << 20:
+        want = moe_oracle.swiglu_expert(P.np64(xn.cpu()), P.np64(sh[0][0].cpu()), P.np64(sh[1][0].cpu()),
+                                        P.np64(sh[2][0].cpu()))
+        P.assert_close("shared_y", P.np64(sh_y.cpu()), want)
