@@ -484,19 +484,27 @@ def measure(wl, steps, warmup, world, pk, e2e_steps):
     ms = total_ms / steps
     alg = algorithmic(cfg, k, copy_rows=not L.gather)
     long_run = total_ms >= 1000.0
-    def bound_s(flops, bytes_):  # the roofline time of one phase: the slower of its two bounds
-        pt = pk["bf16_tflops_sustained"] if long_run else pk["bf16_tflops"]
-        return max(flops / (pt * 1e12), bytes_ / (pk["hbm_gbs"] * 1e9))
-    t_phases = bound_s(alg["gemm_flops"], alg["gemm_bytes"])
-    if L.fuse_shared:  # the shared expert's tiles run in the routed experts' launches, after theirs
-        t_phases += bound_s(alg["shared_flops"], alg["shared_bytes"])
-        alg["gemm_flops"] += alg["shared_flops"]
-        alg["gemm_bytes"] += alg["shared_bytes"]
-    gemm = roofline_of(alg["gemm_flops"], alg["gemm_bytes"], stage_us["grouped_swiglu"], pk, long_run, cfg.dtype)
-    if L.fuse_shared and cfg.dtype == "bf16":
-        gemm["bound_time_frac"] = t_phases / (stage_us["grouped_swiglu"] * 1e-6)
-        gemm["bound_time_note"] = ("(routed experts' roofline time + shared expert's roofline time) / measured time: "
-                                   "the shared tiles follow the routed ones in each launch")
+    alg_r = dict(alg)
+
+    def gemm_roofline(sustained):
+        """The grouped SwiGLU call against the sustained (power-capped) or burst bf16 peak."""
+        a = dict(alg_r)
+
+        def bound_s(flops, bytes_):  # the roofline time of one phase: the slower of its two bounds
+            pt = pk["bf16_tflops_sustained"] if sustained else pk["bf16_tflops"]
+            return max(flops / (pt * 1e12), bytes_ / (pk["hbm_gbs"] * 1e9))
+        t_phases = bound_s(a["gemm_flops"], a["gemm_bytes"])
+        if L.fuse_shared:  # the shared expert's tiles run in the routed experts' launches, after theirs
+            t_phases += bound_s(a["shared_flops"], a["shared_bytes"])
+            a["gemm_flops"] += a["shared_flops"]
+            a["gemm_bytes"] += a["shared_bytes"]
+        r = roofline_of(a["gemm_flops"], a["gemm_bytes"], stage_us["grouped_swiglu"], pk, sustained, cfg.dtype)
+        if L.fuse_shared and cfg.dtype == "bf16":
+            r["bound_time_frac"] = t_phases / (stage_us["grouped_swiglu"] * 1e-6)
+            r["bound_time_note"] = ("(routed experts' roofline time + shared expert's roofline time) / measured "
+                                    "time: the shared tiles follow the routed ones in each launch")
+        return r, a
+    gemm, alg = gemm_roofline(long_run)
     gbs = lambda b, us: b / (us * 1e-6) / 1e9
     hbm = pk["hbm_gbs"]
     copy_us = time_permute_copy(wl, steps)
@@ -506,6 +514,7 @@ def measure(wl, steps, warmup, world, pk, e2e_steps):
         "steps": steps, "launch": mode, "gemm1_rows": "gathered from xn" if L.gather else "permuted copy x_perm",
         "stage_us": {n: round(v, 2) for n, v in stage_us.items()},
         "stage_sum_us": round(sum(stage_us.values()), 2), "stage_us_from": how,
+        "_gemm_sustained": gemm_roofline(True)[0],
         "grouped_gemm": dict(gemm, kernel="moe_grouped_swiglu_shared (routed + shared expert)" if L.fuse_shared
                              else ("moe_grouped_swiglu_gather" if L.gather else "moe_grouped_swiglu"),
                              launches="GEMM1+SwiGLU and GEMM2", us=round(stage_us["grouped_swiglu"], 2),
@@ -535,6 +544,18 @@ def measure(wl, steps, warmup, world, pk, e2e_steps):
     res["e2e"] = {"value": cfg.N * world / (e2e_ms / e2e_steps * 1e-3), "unit": "tokens/s",
                   "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
     return res, total_ms
+
+
+def settle_peak(res, stage_clocks):
+    """A tensor-bound GEMM timed in a stage pass whose clock record shows sw_power_cap ran at
+    the power-capped clock: compare it with the measured sustained bf16 peak (taken under the
+    same cap) rather than the burst one; the burst fraction stays in frac_of_burst."""
+    sus = res.pop("_gemm_sustained")
+    g = res["grouped_gemm"]
+    if g.get("bound") == "tensor" and "sw_power_cap" in (stage_clocks.get("reasons") or []) \
+            and g.get("peak_kind", "").endswith("burst"):
+        keep = {k2: g[k2] for k2 in ("kernel", "launches", "us", "tflops", "algorithmic_gflop", "algorithmic_gb")}
+        res["grouped_gemm"] = dict(sus, **keep, peak_reason="stage pass under sw_power_cap")
 
 
 def max_over_ranks(x, world):
@@ -697,6 +718,7 @@ def main():
         head, total_ms = measure(wl, args.steps, args.warmup, world, pk, args.e2e_steps)
     clocks = clk.summary(head.pop("timed_window"))
     head["clocks_stage_pass"] = clk.summary(head.pop("stage_window"))
+    settle_peak(head, head["clocks_stage_pass"])
     remeasured = clock_problem(clocks)
     # every rank measures again if any rank's record is invalid (the timing has barriers)
     if max_over_ranks(1.0 if remeasured else 0.0, world) > 0:
@@ -705,11 +727,12 @@ def main():
             head, total_ms = measure(wl, args.steps, args.warmup, world, pk, args.e2e_steps)
         clocks = clk.summary(head.pop("timed_window"))
         head["clocks_stage_pass"] = clk.summary(head.pop("stage_window"))
+        settle_peak(head, head["clocks_stage_pass"])
 
     g = head["grouped_gemm"]
     gemm_ms = g["us"] * 1e-3
-    roof = {k2: g[k2] for k2 in ("bound", "achieved", "peak", "unit", "frac", "peak_kind", "bound_time_frac",
-                                 "bound_time_note") if k2 in g}
+    roof = {k2: g[k2] for k2 in ("bound", "achieved", "peak", "unit", "frac", "peak_kind", "peak_reason",
+                                 "frac_of_burst", "bound_time_frac", "bound_time_note") if k2 in g}
     roof.update({"kernel": f"{g['kernel']} ({g['launches']} launches, one call)",
                  "traffic": recorded_traffic(cfg, wl.layer.gather), "traffic_unit": "bytes per call (ncu)",
                  "peak_source": pk_kind, "timed": head["stage_us_from"],
@@ -750,6 +773,7 @@ def main():
                 r2, _ = measure(w2, args.steps, args.warmup, world, pk, args.e2e_steps)
             r2["clocks"] = clk2.summary(r2.pop("timed_window"))
             r2["clocks_stage_pass"] = clk2.summary(r2.pop("stage_window"))
+            settle_peak(r2, r2["clocks_stage_pass"])
             if rank == 0 and c2.bias_steps > 1:
                 r2["load_balance"] = load_balance_trace(w2, c2.bias_steps)
             per[label] = r2

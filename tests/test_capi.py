@@ -54,6 +54,31 @@ def test_workspace_size(lib):
     assert b > 0 and b % 4 == 0 and b <= 128 * 64 * 4
 
 
+def test_new_entry_points_reject_bad_arguments_before_launch(lib):
+    """Only NULL pointers: each call must return its error before touching any pointer."""
+    raw = ctypes.CDLL(moe.lib_path())
+    f = raw.moe_permute_update_bias
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
+                  ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_float, ctypes.c_void_p,
+                  ctypes.c_void_p, ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    # no bias to update
+    assert f(None, 1, 16, 64, None, 2, 8, 16, None, None, None, None, None, None, 0, 1e-3, None, None, None) == -1
+    g = raw.moe_grouped_swiglu_shared
+    g.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int] + \
+        [ctypes.c_void_p] * 5 + [ctypes.c_void_p, ctypes.c_int] + [ctypes.c_void_p] * 6
+    g.restype = ctypes.c_int
+    assert g(None, None, 0, 0, 128, 128, None, None, None, None, None, None, 0, None, None, None, None, None,
+             None) == -1                                            # G < 1
+    assert g(None, None, 4, 0, 100, 128, None, None, None, None, None, None, 0, None, None, None, None, None,
+             None) == -2                                            # D not a multiple of 64
+    assert g(None, None, 4, 64, 128, 128, None, None, None, None, None, None, 0, None, None, None, None, None,
+             None) == -1                                            # routed rows but no operands
+    assert g(None, None, 4, 0, 128, 128, None, None, None, None, None, None, 8, None, None, None, None, None,
+             None) == -1                                            # shared rows but no operands
+
+
 def test_expert_capacity_through_the_abi(lib):
     """ceil(C N k / E), capped at N k; -1 for arguments outside the domain."""
     raw = ctypes.CDLL(moe.lib_path())
