@@ -60,6 +60,8 @@ def recorded_traffic(cfg, gather):
     """ncu DRAM bytes of one grouped SwiGLU call (the row-gathering variant when `gather`), if
     recorded for this workload and the kernel sources are unchanged since (else None)."""
     import hashlib
+    if synth.CONFIGS.get(cfg.name) != cfg:  # a scaled workload: the record is for the full size
+        return None
     suffix = "_gather" if gather else ""
     path = os.path.join(ROOT, "profiles", f"grouped_gemm_{cfg.name}{suffix}_traffic.txt")
     if not os.path.exists(path):
@@ -685,6 +687,9 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", action="store_true", help="measure the headline workload only")
+    ap.add_argument("--override", default="",
+                    help="comma-separated size overrides of the configuration, e.g. N=512,E=32 (a scaled "
+                         "workload of the same recipe, for small profiling captures)")
     rows = ap.add_mutually_exclusive_group()
     rows.add_argument("--permute-copy", action="store_true",
                       help="the permute writes the permuted rows x_perm and GEMM1 loads them by TMA")
@@ -695,6 +700,9 @@ def main():
                            "chooses by size)")
     args = ap.parse_args()
     cfg = synth.CONFIGS[args.config]
+    if args.override:
+        kw = {kv.split("=")[0]: int(kv.split("=")[1]) for kv in args.override.split(",")}
+        cfg = synth.scaled(cfg, **kw)
     k = args.k or cfg.k
     if args.impl == "reference":
         reference_arm(args, cfg, k)
@@ -776,6 +784,8 @@ def main():
             settle_peak(r2, r2["clocks_stage_pass"])
             if rank == 0 and c2.bias_steps > 1:
                 r2["load_balance"] = load_balance_trace(w2, c2.bias_steps)
+            if rank == 0 and world == 1 and not args.no_cpu_baseline:
+                r2["cpu_baseline"] = cpu_baseline(c2, kk, budget_s=3.0, max_runs=10)
             per[label] = r2
             del w2
             torch.cuda.empty_cache()
