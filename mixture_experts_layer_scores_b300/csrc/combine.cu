@@ -43,73 +43,86 @@ struct Vec<float> {
   }
 };
 
-// One CTA per (token, column chunk of CHB bytes); thread i owns the chunk's 16-byte vector i.
-// Each thread starts async copies (cp.async, L2 only) of its vector from the token's k
-// expert rows and its shared-expert and residual rows into shared memory, waits for its own
-// copies, then weights and sums them in slot order and writes out.  The copies keep k + 2
-// loads per thread in flight without holding registers for them, and at 20 KB of shared
-// memory per CTA (k = 8) about ten CTAs share an SM: enough requests in flight to keep
-// HBM busy, which a loop of dependent register loads over j is not.
+// One CTA per (TPC tokens, column chunk of CHB bytes); thread i owns the chunk's 16-byte
+// vector i of each of its tokens.  Each thread starts async copies (cp.async, L2 only) of its
+// vectors from every token's k expert rows and its shared-expert and residual rows into shared
+// memory, waits for its own copies, then weights and sums them in slot order and writes out.
+// The copies keep TPC * (k + 2) loads per thread in flight without holding registers for them;
+// TPC grows for small k (k = 2: two tokens, eight copies) so that a CTA's one round trip for
+// its tokens' row indices and gates is shared by enough data loads.  A loop of dependent
+// register loads over j does not keep HBM busy.
 constexpr int CHB = 2048;
 constexpr int THREADS = CHB / 16;
 
+// tokens per CTA for k experts per token: at least ~8 copies in flight per thread
+inline int tokens_per_cta(int k) { return k >= 6 ? 1 : (8 + k + 1) / (k + 2); }
+
 template <typename T>
 __global__ void __launch_bounds__(THREADS) combine_kernel(const T* __restrict__ y, const int32_t* __restrict__ row_map,
-                                                          const float* __restrict__ gate, int k, int D,
-                                                          const T* __restrict__ shared_y,
+                                                          const float* __restrict__ gate, int N, int k, int D,
+                                                          int tpc, const T* __restrict__ shared_y,
                                                           const T* __restrict__ residual, T* __restrict__ out) {
   using namespace tc;
   constexpr int W = Vec<T>::W;
-  extern __shared__ __align__(16) uint8_t stage[];  // [k + 2][CHB]: expert rows, shared, residual
-  __shared__ int rows[MOE_MAX_TOPK];
-  __shared__ float gs[MOE_MAX_TOPK];
+  extern __shared__ __align__(16) uint8_t stage[];  // [tpc][k + 2][CHB]: expert rows, shared, residual
+  __shared__ int rows[4 * MOE_MAX_TOPK];
+  __shared__ float gs[4 * MOE_MAX_TOPK];
   const int rowbytes = D * (int)sizeof(T);
   const int nch = (rowbytes + CHB - 1) / CHB;
-  const int n = blockIdx.x / nch, c = blockIdx.x % nch;
+  const int n0 = (blockIdx.x / nch) * tpc, c = blockIdx.x % nch;
+  const int nt = min(tpc, N - n0);  // tokens of this CTA
   grid_dep_wait();
   grid_dep_launch();
-  if (threadIdx.x < k) {
-    rows[threadIdx.x] = row_map[(size_t)n * k + threadIdx.x];
-    gs[threadIdx.x] = gate[(size_t)n * k + threadIdx.x];
+  if (threadIdx.x < nt * k) {
+    rows[threadIdx.x] = row_map[(size_t)n0 * k + threadIdx.x];
+    gs[threadIdx.x] = gate[(size_t)n0 * k + threadIdx.x];
   }
   __syncthreads();
   const int off = c * CHB + threadIdx.x * 16;
   if (off >= rowbytes) return;
+  const int per = (k + 2) * CHB;  // shared-memory bytes of one token
   const uint32_t mine = smem_u32(stage) + threadIdx.x * 16;
   const uint8_t* yb = reinterpret_cast<const uint8_t*>(y);
-  for (int j = 0; j < k; ++j)
-    if (rows[j] >= 0) cp_async_16(mine + j * CHB, yb + (size_t)rows[j] * rowbytes + off, 16);
-  if (shared_y)
-    cp_async_16(mine + k * CHB, reinterpret_cast<const uint8_t*>(shared_y) + (size_t)n * rowbytes + off, 16);
-  if (residual)
-    cp_async_16(mine + (k + 1) * CHB, reinterpret_cast<const uint8_t*>(residual) + (size_t)n * rowbytes + off, 16);
+  for (int t = 0; t < nt; ++t) {
+    const int n = n0 + t;
+    for (int j = 0; j < k; ++j)
+      if (rows[t * k + j] >= 0) cp_async_16(mine + t * per + j * CHB, yb + (size_t)rows[t * k + j] * rowbytes + off, 16);
+    if (shared_y)
+      cp_async_16(mine + t * per + k * CHB, reinterpret_cast<const uint8_t*>(shared_y) + (size_t)n * rowbytes + off,
+                  16);
+    if (residual)
+      cp_async_16(mine + t * per + (k + 1) * CHB,
+                  reinterpret_cast<const uint8_t*>(residual) + (size_t)n * rowbytes + off, 16);
+  }
   cp_async_commit();
   cp_async_wait<0>();
-  const uint8_t* v = stage + threadIdx.x * 16;
-  float acc[W];
+  for (int t = 0; t < nt; ++t) {
+    const uint8_t* v = stage + t * per + threadIdx.x * 16;
+    float acc[W];
 #pragma unroll
-  for (int i = 0; i < W; ++i) acc[i] = 0.f;
-  for (int j = 0; j < k; ++j) {
-    if (rows[j] < 0) continue;  // dropped slot
-    float f[W];
-    Vec<T>::load_shared(v + j * CHB, f);
-    const float g = gs[j];
+    for (int i = 0; i < W; ++i) acc[i] = 0.f;
+    for (int j = 0; j < k; ++j) {
+      if (rows[t * k + j] < 0) continue;  // dropped slot
+      float f[W];
+      Vec<T>::load_shared(v + j * CHB, f);
+      const float g = gs[t * k + j];
 #pragma unroll
-    for (int i = 0; i < W; ++i) acc[i] = fmaf(g, f[i], acc[i]);
+      for (int i = 0; i < W; ++i) acc[i] = fmaf(g, f[i], acc[i]);
+    }
+    if (shared_y) {
+      float f[W];
+      Vec<T>::load_shared(v + k * CHB, f);
+#pragma unroll
+      for (int i = 0; i < W; ++i) acc[i] += f[i];
+    }
+    if (residual) {
+      float f[W];
+      Vec<T>::load_shared(v + (k + 1) * CHB, f);
+#pragma unroll
+      for (int i = 0; i < W; ++i) acc[i] += f[i];
+    }
+    Vec<T>::store(reinterpret_cast<uint8_t*>(out) + (size_t)(n0 + t) * rowbytes + off, acc);
   }
-  if (shared_y) {
-    float f[W];
-    Vec<T>::load_shared(v + k * CHB, f);
-#pragma unroll
-    for (int i = 0; i < W; ++i) acc[i] += f[i];
-  }
-  if (residual) {
-    float f[W];
-    Vec<T>::load_shared(v + (k + 1) * CHB, f);
-#pragma unroll
-    for (int i = 0; i < W; ++i) acc[i] += f[i];
-  }
-  Vec<T>::store(reinterpret_cast<uint8_t*>(out) + (size_t)n * rowbytes + off, acc);
 }
 
 __global__ void bias_update_kernel(const int32_t* __restrict__ counts, int E, long long total,
@@ -155,18 +168,20 @@ extern "C" moe_status_t moe_unpermute_combine(const void* y_perm, const int32_t*
   if (!aligned16(y_perm) || !aligned16(out) || (shared_y && !aligned16(shared_y)) ||
       (residual && !aligned16(residual)))
     return MOE_ERR_INVALID_ARG;
-  const long long blocks = (long long)N * ((D * esize + CHB - 1) / CHB);
+  const int tpc = tokens_per_cta(k);
+  const long long blocks = (long long)((N + tpc - 1) / tpc) * ((D * esize + CHB - 1) / CHB);
   if (blocks > 0x7fffffffll) return MOE_ERR_UNSUPPORTED;
   cudaStream_t s = as_cuda(stream);
-  const size_t smem = (size_t)(k + 2) * CHB;  // at most 36 KB: no opt-in needed
+  const size_t smem = (size_t)tpc * (k + 2) * CHB;  // at most 36 KB: no opt-in needed
   if (dtype == MOE_BF16)
     return launch_kernel(combine_kernel<__nv_bfloat16>, dim3((unsigned)blocks), dim3(THREADS), smem, s,
-                         static_cast<const __nv_bfloat16*>(y_perm), row_map, topk_gate, k, D,
+                         static_cast<const __nv_bfloat16*>(y_perm), row_map, topk_gate, N, k, D, tpc,
                          static_cast<const __nv_bfloat16*>(shared_y), static_cast<const __nv_bfloat16*>(residual),
                          static_cast<__nv_bfloat16*>(out));
   return launch_kernel(combine_kernel<float>, dim3((unsigned)blocks), dim3(THREADS), smem, s,
-                       static_cast<const float*>(y_perm), row_map, topk_gate, k, D, static_cast<const float*>(shared_y),
-                       static_cast<const float*>(residual), static_cast<float*>(out));
+                       static_cast<const float*>(y_perm), row_map, topk_gate, N, k, D, tpc,
+                       static_cast<const float*>(shared_y), static_cast<const float*>(residual),
+                       static_cast<float*>(out));
 }
 
 extern "C" moe_status_t moe_bias_update(const int32_t* counts, int E, int64_t total_assignments,

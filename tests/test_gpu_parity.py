@@ -314,6 +314,9 @@ COMBINE_CASES = {
     "bf16_D64_k16_bare": (torch.bfloat16, 149, 64, 16, False, False),
     "bf16_D7168_k8_shared": (torch.bfloat16, 40, 7168, 8, True, False),
     "bf16_single_token": (torch.bfloat16, 1, 2048, 4, True, True),
+    # small k: several tokens per CTA (two at k = 2, three at k = 1), with a partial last group
+    "bf16_D4096_k2_residual": (torch.bfloat16, 257, 4096, 2, False, True),
+    "bf16_D2048_k1_shared_residual": (torch.bfloat16, 100, 2048, 1, True, True),
 }
 
 
