@@ -395,3 +395,26 @@ def test_shared_expert_in_routed_launches(N, D, E, F, k):
         want = moe_oracle.swiglu_expert(P.np64(xn.cpu()), P.np64(sh[0][0].cpu()), P.np64(sh[1][0].cpu()),
                                         P.np64(sh[2][0].cpu()))
         P.assert_close("shared_y", P.np64(sh_y.cpu()), want)
+
+
+def test_gather_repeated_back_to_back():
+    """The gathering GEMM1 with CTA-pair GEMM2 (experts averaging >= 256 rows), 30 calls back
+    to back: every call bit-identical to the copy path, no device status raised (the CTAs of a
+    pair must build the same tile list every time, or one waits for the other until its
+    bounded wait runs out)."""
+    N, D, E, F, k = 4096, 512, 16, 256, 2
+    cfg = synth.scaled(synth.CONFIGS["handbook"], N=N, D=D, E=E, F=F, k=k)
+    xn, _ = synth.make_tokens(cfg, "cuda")
+    wg, wu, wd = synth.make_experts(cfg, "cuda")
+    rng = np.random.default_rng(3)
+    idx = torch.from_numpy(np.stack([rng.choice(E, k, replace=False) for _ in range(N)]).astype(np.int32)).cuda()
+    counts, offsets, row_map, perm, x_perm = moe.moe_permute(xn, idx, E)
+    ref = moe.moe_grouped_swiglu(x_perm, offsets, wg, wu, wd)
+    h = torch.empty(N * k, F, dtype=torch.bfloat16, device="cuda")
+    outs = [torch.empty(N * k, D, dtype=torch.bfloat16, device="cuda") for _ in range(30)]
+    for o in outs:
+        moe.moe_grouped_swiglu_gather(xn, perm, offsets, wg, wu, wd, h, o)
+    torch.cuda.synchronize()
+    assert moe.last_device_status() == 0
+    for o in outs:
+        assert torch.equal(o, ref)
