@@ -945,7 +945,7 @@ namespace simt {
 
 // fp32 grouped SwiGLU on CUDA cores: 64 x 64 output tiles, 256 threads with 4 x 4 outputs
 // each, 32-wide K slices staged in shared memory (k-major, so a thread reads four rows or
-// four columns as one float4).  Every output is one fp32 FMA chain over K in index order
+// four columns as one float4), the next slice loaded into registers during the FMAs.  Every output is one fp32 FMA chain over K in index order
 // (bit-identical to a plain dot-product loop).  Tiles are (group, 64-row block, column
 // block); a CTA finds its group by walking the offsets.
 constexpr int TM = 64, TN = 64, TK = 32, PAD = 4;
@@ -977,22 +977,36 @@ __device__ __forceinline__ SimtTile simt_tile(int t, const int32_t* __restrict__
   return r;
 }
 
-// rows [row0, row0 + rows) x cols [k0, k0 + TK) of a row-major [*, ld] matrix into dst[k][m]
-// (transposed), zero beyond `rows` rows.
-__device__ __forceinline__ void stage_t(float (*dst)[TM + PAD], const float* __restrict__ src, int ld, int row0,
-                                        int rows, int k0) {
-  for (int i = threadIdx.x; i < TM * TK / 4; i += blockDim.x) {
-    const int m = i / (TK / 4), kq = (i % (TK / 4)) * 4;
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (m < rows) v = *reinterpret_cast<const float4*>(src + (size_t)(row0 + m) * ld + k0 + kq);
-    dst[kq + 0][m] = v.x;
-    dst[kq + 1][m] = v.y;
-    dst[kq + 2][m] = v.z;
-    dst[kq + 3][m] = v.w;
+// One thread's share of a 64-row x TK-column slice of a row-major [*, ld] matrix (rows
+// [row0, row0 + rows), columns [k0, k0 + TK); zero beyond `rows`): TM * TK / 4 / 256 float4.
+constexpr int SLICE_V = TM * TK / 4 / 256;
+struct Slice {
+  float4 v[SLICE_V];
+  __device__ __forceinline__ void load(const float* __restrict__ src, int ld, int row0, int rows, int k0) {
+#pragma unroll
+    for (int q = 0; q < SLICE_V; ++q) {
+      const int i = threadIdx.x + q * 256;
+      const int m = i / (TK / 4), kq = (i % (TK / 4)) * 4;
+      v[q] = m < rows ? *reinterpret_cast<const float4*>(src + (size_t)(row0 + m) * ld + k0 + kq)
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
   }
-}
+  // into dst[k][m] (k-major, so the compute loop reads four rows or columns as one float4)
+  __device__ __forceinline__ void store(float (*dst)[TM + PAD]) const {
+#pragma unroll
+    for (int q = 0; q < SLICE_V; ++q) {
+      const int i = threadIdx.x + q * 256;
+      const int m = i / (TK / 4), kq = (i % (TK / 4)) * 4;
+      dst[kq + 0][m] = v[q].x;
+      dst[kq + 1][m] = v[q].y;
+      dst[kq + 2][m] = v[q].z;
+      dst[kq + 3][m] = v[q].w;
+    }
+  }
+};
 
-// H[r, f] = SiLU(x_r . W_gate[g, f]) * (x_r . W_up[g, f])
+// H[r, f] = SiLU(x_r . W_gate[g, f]) * (x_r . W_up[g, f]).  The next K slice is loaded into
+// registers while the current one is multiplied out of shared memory.
 __global__ void __launch_bounds__(256, 2) swiglu_up_kernel(const float* __restrict__ x, const int32_t* __restrict__ offsets,
                                                         int G, int M, int D, int F, const float* __restrict__ wg,
                                                         const float* __restrict__ wu, float* __restrict__ h) {
@@ -1007,11 +1021,20 @@ __global__ void __launch_bounds__(256, 2) swiglu_up_kernel(const float* __restri
   const float* wgg = wg + ((size_t)tl.g * F + tl.col0) * D;
   const float* wug = wu + ((size_t)tl.g * F + tl.col0) * D;
   float ag[4][4] = {}, au[4][4] = {};
+  Slice sx, sg, su;
+  sx.load(x, D, tl.row0, tl.rows, 0);
+  sg.load(wgg, D, 0, ncols, 0);
+  su.load(wug, D, 0, ncols, 0);
   for (int k0 = 0; k0 < D; k0 += TK) {
-    stage_t(xs, x, D, tl.row0, tl.rows, k0);
-    stage_t(gs, wgg, D, 0, ncols, k0);
-    stage_t(us, wug, D, 0, ncols, k0);
+    sx.store(xs);
+    sg.store(gs);
+    su.store(us);
     __syncthreads();
+    if (k0 + TK < D) {  // next slice in flight during the FMAs
+      sx.load(x, D, tl.row0, tl.rows, k0 + TK);
+      sg.load(wgg, D, 0, ncols, k0 + TK);
+      su.load(wug, D, 0, ncols, k0 + TK);
+    }
 #pragma unroll 8
     for (int k = 0; k < TK; ++k) {
       const float4 a = *reinterpret_cast<const float4*>(&xs[k][ty * 4]);
@@ -1057,10 +1080,17 @@ __global__ void __launch_bounds__(256, 2) swiglu_down_kernel(const float* __rest
   const int ncols = min(TN, D - tl.col0);
   const float* wdg = wd + ((size_t)tl.g * D + tl.col0) * F;
   float acc[4][4] = {};
+  Slice sh, sd;
+  sh.load(h, F, tl.row0, tl.rows, 0);
+  sd.load(wdg, F, 0, ncols, 0);
   for (int k0 = 0; k0 < F; k0 += TK) {
-    stage_t(hs, h, F, tl.row0, tl.rows, k0);
-    stage_t(ds, wdg, F, 0, ncols, k0);
+    sh.store(hs);
+    sd.store(ds);
     __syncthreads();
+    if (k0 + TK < F) {
+      sh.load(h, F, tl.row0, tl.rows, k0 + TK);
+      sd.load(wdg, F, 0, ncols, k0 + TK);
+    }
 #pragma unroll 8
     for (int k = 0; k < TK; ++k) {
       const float4 a = *reinterpret_cast<const float4*>(&hs[k][ty * 4]);
