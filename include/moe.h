@@ -319,21 +319,25 @@ moe_status_t moe_grouped_swiglu_ex(const void* x_perm, moe_dtype_t dtype, const 
  * visits, added to the routed sum) and "Concept" (every expert a SwiGLU FFN).  The shared
  * expert's 128-row tiles follow the routed experts' tiles in each launch's tile list, so it
  * needs no launches of its own and fills the routed tiles' last wave.  Same bits as
- * moe_grouped_swiglu on the routed rows followed by moe_grouped_swiglu with G = 1, offsets
- * {0, N} on xn.
+ * moe_grouped_swiglu (or moe_grouped_swiglu_gather) on the routed rows followed by
+ * moe_grouped_swiglu with G = 1, offsets {0, N} on xn.
  *   x_perm, offsets, G, M_total, D, F, w_gate, w_up, w_down, h_workspace, y_perm:
  *                      as moe_grouped_swiglu (bf16 only)
+ *   perm_token [M_total] DEVICE int32 or NULL: non-NULL gathers the routed rows from
+ *                      xn[perm_token[i]] as moe_grouped_swiglu_gather does (x_perm is then
+ *                      not read and may be NULL); NULL reads them from x_perm
  *   xn        [N, D]   the shared expert's rows (norm(h)); N = 0: no shared expert
  *   ws_gate, ws_up [F, D], ws_down [D, F]  the shared expert's weights (the same d_ff F)
  *   hs_workspace [N, F] scratch; shared_y [N, D] out
  * When the routed experts average 256 rows or more they run on the CTA-pair kernels first and
- * the shared expert runs alone in the one-CTA kernel.  MOE_ERR_UNSUPPORTED when the shared
- * gate and up weights cannot be addressed as the two planes of one tensor map (their
- * distance in memory below F*D*2 bytes or not a multiple of 16).
+ * the shared expert runs alone in the one-CTA kernel.  MOE_ERR_INVALID_ARG for a non-NULL
+ * perm_token with N = 0 and M_total > 0 (rows to gather, no tokens); MOE_ERR_UNSUPPORTED
+ * when the shared gate and up weights cannot be addressed as the two planes of one tensor
+ * map (their distance in memory below F*D*2 bytes or not a multiple of 16).
  */
-moe_status_t moe_grouped_swiglu_shared(const void* x_perm, const int32_t* offsets, int G, int M_total,
-                                       int D, int F, const void* w_gate, const void* w_up,
-                                       const void* w_down, void* h_workspace, void* y_perm,
+moe_status_t moe_grouped_swiglu_shared(const void* x_perm, const int32_t* perm_token, const int32_t* offsets,
+                                       int G, int M_total, int D, int F, const void* w_gate,
+                                       const void* w_up, const void* w_down, void* h_workspace, void* y_perm,
                                        const void* xn, int N, const void* ws_gate, const void* ws_up,
                                        const void* ws_down, void* hs_workspace, void* shared_y,
                                        moe_stream_t stream);

@@ -12,7 +12,8 @@
 //   warp 0      one lane issues TMA loads (128B-swizzled K-major tiles) into a
 //               4-stage shared-memory ring guarded by full/empty mbarriers;
 //   warp 1      allocates 512 TMEM columns (two 256-column fp32 accumulators) and
-//               one lane issues tcgen05.mma (M=128, N=256, K=16) and tcgen05.commit;
+//               one lane issues tcgen05.mma (M=128, or M=64 for a tile of at most 64
+//               rows; N=256, K=16) and tcgen05.commit;
 //   warps 2..5  drain an accumulator with tcgen05.ld while the MMA warp fills the
 //               other one, apply the epilogue and store bf16 rows, masking rows past
 //               the expert's segment and columns past the output width.
@@ -48,6 +49,16 @@ constexpr int MAX_GROUPS = 1024;
 constexpr int STAGING_BYTES = 32 * 128;  // one 32-row x 64-column bf16 output block
 
 constexpr uint32_t IDESC = idesc_bf16(BM, BN);
+// A tile with at most 64 rows (an expert's last rows, a small expert) is a half tile: one
+// M = 64 MMA per K step instead of an M = 128 one over 64 or more padded rows.  Measured on
+// B300 (N = 256, K = 16) it takes the same 128 cycles as M = 128 but draws less power, which
+// is what sets the speed of these launches once the GPU runs at its power limit.  (The
+// weight-stationary M = 64 form takes 80 cycles but drew more power: slower at the limit.)
+// Measured accumulator layout (M = 64, one CTA): row r sits in TMEM lane 32 * (r / 16) +
+// r % 16, at the same columns as for M = 128.
+constexpr int HALF_ROWS = BM / 2;
+constexpr uint32_t IDESC_HALF = idesc_bf16(HALF_ROWS, BN);
+constexpr int A_BOX = HALF_ROWS;        // rows per A copy: one for a half tile, two for a full one
 
 // Most CTAs a grouped GEMM launch may use (0 = every SM); set for one call by
 // moe_grouped_swiglu_ex so that other work can run on the remaining SMs.
@@ -232,7 +243,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
   const uint32_t tmem_base = *tmem_holder;
   ExtraList XL;
   XL.routed = tile_start[G];
-  XL.M2 = MODE != 2 ? M2 : 0;
+  XL.M2 = M2;
   XL.NX = XL.M2 > 0 ? ((XL.M2 + BM - 1) / BM) * NB : 0;
   const int total_tiles = XL.total();
   auto tile_at = [&](int tile) { return decode_list(tile, XL, tile_start, G, offsets, M_total, NB); };
@@ -277,6 +288,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+        const uint32_t idesc = tile_at(tile).rows <= HALF_ROWS ? IDESC_HALF : IDESC;
         if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, status, true)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
@@ -288,7 +300,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
           const uint32_t b_base = a_base + A_BYTES;
 #pragma unroll
           for (int k = 0; k < BK / UK; ++k)
-            tc_mma(d_tmem, sw128_desc(a_base + k * UK * 2), sw128_desc(b_base + k * UK * 2), IDESC,
+            tc_mma(d_tmem, sw128_desc(a_base + k * UK * 2), sw128_desc(b_base + k * UK * 2), idesc,
                    (kb | k) != 0 ? 1u : 0u);
           tc_commit(empty_bar(stage));
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -309,11 +321,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
       for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
         const Tile tl = tile_at(tile);
         const CUtensorMap* ma = tl.x ? &map_a2 : &map_a;
+        const bool half = tl.rows <= HALF_ROWS;  // the M = 64 MMA reads the first 64 rows only
         bool ok = true;
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, status, true)) { ok = false; break; }
-          mbar_expect_tx(full_bar(stage), A_BYTES);
-          tma_load_2d(smem_u32(smem + stage * STAGE_BYTES), ma, kb * BK, tl.row0, full_bar(stage));
+          const uint32_t dst = smem_u32(smem + stage * STAGE_BYTES);
+          mbar_expect_tx(full_bar(stage), half ? A_BYTES / 2 : A_BYTES);
+          tma_load_2d(dst, ma, kb * BK, tl.row0, full_bar(stage));
+          if (!half) tma_load_2d(dst + A_BYTES / 2, ma, kb * BK, tl.row0 + A_BOX, full_bar(stage));
           issued |= 1u << stage;
           issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -337,11 +352,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
     // dependent loads while earlier stages still wait for its arrival.
     Tile tl_next{};
     int tok_next[8];
-    auto load_tokens = [&]() {
+    auto load_tokens = [&]() {  // the extra group's rows are xn's own rows, in order
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int r = 32 * w + 4 * i + (lane >> 3);
-        tok_next[i] = r < tl_next.rows ? __ldg(perm + tl_next.row0 + r) : -1;
+        tok_next[i] = r < tl_next.rows ? (tl_next.x ? tl_next.row0 + r : __ldg(perm + tl_next.row0 + r)) : -1;
       }
     };
     const int kb_decode = KB > 2 ? 1 : 0, kb_tokens = KB > 2 ? 2 : KB - 1;
@@ -366,11 +381,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
         doff[i] = (uint32_t)r * 128u + ((uint32_t)(c ^ (r & 7)) << 4);
       }
       const bool more = tile + (int)gridDim.x < total_tiles;
+      const bool idle = tl.rows <= HALF_ROWS && w >= 2;  // rows 64..127: not read by the M = 64 MMA
       for (int kb = 0; kb < KB; ++kb) {
         if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, status, true)) { ok = false; break; }
         const uint32_t base = smem_u32(smem + stage * STAGE_BYTES);
+        if (!idle) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) cp_async_16(base + doff[i], src[i] + kb * BK, ((live >> i) & 1u) << 4);
+          for (int i = 0; i < 8; ++i) cp_async_16(base + doff[i], src[i] + kb * BK, ((live >> i) & 1u) << 4);
+        }
         cp_async_commit();
         if (++pend > LAG) {  // the oldest stage's copies are complete once LAG groups remain
           cp_async_wait<LAG>();
@@ -398,7 +416,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
     // swizzled shared-memory buffer and one TMA bulk store (row by row from registers when
     // the block crosses the end of its group's rows), as in the CTA-pair kernel.
     const int q = warp & 3;  // TMEM lane quarter this warp may access
-    const int row_local = q * 32 + lane;
     const uint32_t my_staging = smem_u32(staging) + (uint32_t)(q * nbuf * STAGING_BYTES);
     int acc = 0, bi = 0, stores = 0;
     uint32_t acc_phase = 0;
@@ -411,8 +428,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-      const bool valid = row_local < tl.rows;
-      const bool whole = q * 32 + 32 <= tl.rows;  // warp-uniform
+      // a half tile's rows 16q..16q+15 are in this warp's lanes 0..15
+      const bool half = tl.rows <= HALF_ROWS;
+      const int r0 = half ? q * 16 : q * 32;  // first tile row of this warp
+      const bool valid = (!half || lane < 16) && r0 + lane < tl.rows;
+      const bool whole = !half && r0 + 32 <= tl.rows;  // warp-uniform
 #pragma unroll 1
       for (int u = 0; u < TN / 64; ++u) {
         const int ocol = u * 64;
@@ -461,13 +481,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_2d(mo, tl.nb * TN + ocol, tl.row0 + q * 32, buf);
+            tma_store_2d(mo, tl.nb * TN + ocol, tl.row0 + r0, buf);
             bulk_commit();
           }
           ++stores;
           if (++bi == nbuf) bi = 0;
         } else if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(optr + (size_t)(tl.row0 + row_local) * NOUT + tl.nb * TN + ocol);
+          uint4* dst = reinterpret_cast<uint4*>(optr + (size_t)(tl.row0 + r0 + lane) * NOUT + tl.nb * TN + ocol);
 #pragma unroll
           for (int c = 0; c < 8; ++c) dst[c] = packed[c];
         }
@@ -908,7 +928,7 @@ moe_status_t launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorM
     return MOE_ERR_CUDA;
   const int TN = MODE != 1 ? BN / 2 : BN;
   const long long NB = (NOUT + TN - 1) / TN;
-  const int M2 = MODE != 2 ? x.M : 0;
+  const int M2 = x.M;
   const long long max_tiles = ((long long)(M_total + BM - 1) / BM + G) * NB + ((long long)(M2 + BM - 1) / BM) * NB;
   const int grid = (int)std::min<long long>(max_tiles, (long long)cta_cap());
   return launch_kernel(kern, dim3(grid), dim3(kThreads<MODE>), smem, s, a, b0, b1, out_map, offsets, G, M_total, K,
@@ -1189,10 +1209,10 @@ extern "C" moe_status_t moe_grouped_swiglu(const void* x_perm, moe_dtype_t dtype
     return tc::launch_pair<1>(mh, mh2, md, md, myo, 0, offsets, G, M_total, F, D, y_perm, status, s);
   }
   CUtensorMap ma, mg, mu, mh, md, mho, myo;
-  if (!tc::make_map_bf16(&ma, x_perm, (uint64_t)M_total, (uint64_t)D, tc::BM) ||
+  if (!tc::make_map_bf16(&ma, x_perm, (uint64_t)M_total, (uint64_t)D, tc::A_BOX) ||
       !tc::make_map_bf16(&mg, w_gate, (uint64_t)G * F, (uint64_t)D, tc::BN / 2) ||
       !tc::make_map_bf16(&mu, w_up, (uint64_t)G * F, (uint64_t)D, tc::BN / 2) ||
-      !tc::make_map_bf16(&mh, h_workspace, (uint64_t)M_total, (uint64_t)F, tc::BM) ||
+      !tc::make_map_bf16(&mh, h_workspace, (uint64_t)M_total, (uint64_t)F, tc::A_BOX) ||
       !tc::make_map_bf16(&md, w_down, (uint64_t)G * D, (uint64_t)F, tc::BN) ||
       !tc::make_map_bf16(&mho, h_workspace, (uint64_t)M_total, (uint64_t)F, 32) ||
       !tc::make_map_bf16(&myo, y_perm, (uint64_t)M_total, (uint64_t)D, 32))
@@ -1220,32 +1240,37 @@ extern "C" moe_status_t moe_grouped_swiglu_ex(const void* x_perm, moe_dtype_t dt
   return st;
 }
 
-extern "C" moe_status_t moe_grouped_swiglu_shared(const void* x_perm, const int32_t* offsets, int G, int M_total,
-                                                  int D, int F, const void* w_gate, const void* w_up,
-                                                  const void* w_down, void* h_workspace, void* y_perm,
-                                                  const void* xn, int N, const void* ws_gate, const void* ws_up,
-                                                  const void* ws_down, void* hs_workspace, void* shared_y,
-                                                  moe_stream_t stream) {
+extern "C" moe_status_t moe_grouped_swiglu_shared(const void* x_perm, const int32_t* perm_token,
+                                                  const int32_t* offsets, int G, int M_total, int D, int F,
+                                                  const void* w_gate, const void* w_up, const void* w_down,
+                                                  void* h_workspace, void* y_perm, const void* xn, int N,
+                                                  const void* ws_gate, const void* ws_up, const void* ws_down,
+                                                  void* hs_workspace, void* shared_y, moe_stream_t stream) {
   using namespace moe;
+  const bool gather = perm_token != nullptr;  // routed rows read from xn through perm_token
   if (G < 1 || M_total < 0 || D <= 0 || F <= 0 || N < 0) return MOE_ERR_INVALID_ARG;
   if (D % 64 != 0 || F % 64 != 0 || G > tc::MAX_GROUPS) return MOE_ERR_UNSUPPORTED;
   if ((long long)G * F >= (1LL << 31) || (long long)G * D >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
-  if (M_total > 0 && (!x_perm || !offsets || !w_gate || !w_up || !w_down || !h_workspace || !y_perm))
+  if (M_total > 0 && ((!gather && !x_perm) || !offsets || !w_gate || !w_up || !w_down || !h_workspace || !y_perm))
     return MOE_ERR_INVALID_ARG;
+  if (gather && M_total > 0 && (!xn || N < 1)) return MOE_ERR_INVALID_ARG;
   if (N > 0 && (!xn || !ws_gate || !ws_up || !ws_down || !hs_workspace || !shared_y)) return MOE_ERR_INVALID_ARG;
   for (const void* p : {x_perm, (const void*)w_gate, w_up, w_down, (const void*)h_workspace, (const void*)y_perm, xn,
                         ws_gate, ws_up, ws_down, (const void*)hs_workspace, (const void*)shared_y})
     if (p && !aligned16(p)) return MOE_ERR_INVALID_ARG;
-  if (N == 0)
-    return moe_grouped_swiglu(x_perm, MOE_BF16, offsets, G, M_total, D, F, w_gate, w_up, w_down, h_workspace, y_perm,
-                              stream);
+  auto routed_alone = [&]() {
+    return gather ? moe_grouped_swiglu_gather(xn, N, perm_token, offsets, G, M_total, D, F, w_gate, w_up, w_down,
+                                              h_workspace, y_perm, stream)
+                  : moe_grouped_swiglu(x_perm, MOE_BF16, offsets, G, M_total, D, F, w_gate, w_up, w_down,
+                                       h_workspace, y_perm, stream);
+  };
+  if (N == 0) return routed_alone();
   if (!offsets) return MOE_ERR_INVALID_ARG;
   // Routed experts large enough for CTA pairs run on the pair kernels first; the shared
   // expert then runs alone as the extra group of one-CTA launches with no routed rows.
   const bool separate = M_total == 0 || tc::use_pair(G, M_total);
   if (separate && M_total > 0) {
-    const moe_status_t st = moe_grouped_swiglu(x_perm, MOE_BF16, offsets, G, M_total, D, F, w_gate, w_up, w_down,
-                                               h_workspace, y_perm, stream);
+    const moe_status_t st = routed_alone();
     if (st != MOE_OK) return st;
   }
   const int Mr = separate ? 0 : M_total;  // routed rows in these launches
@@ -1255,8 +1280,8 @@ extern "C" moe_status_t moe_grouped_swiglu_shared(const void* x_perm, const int3
   CUtensorMap ma, mg, mu, mh, md, mho, myo, mgu;
   CUtensorMap xa, xgu, xh, xd, xho, xyo;
   int planes = 0, xplanes = 0;
-  if (!tc::make_map_bf16(&xa, xn, (uint64_t)N, (uint64_t)D, tc::BM) ||
-      !tc::make_map_bf16(&xh, hs_workspace, (uint64_t)N, (uint64_t)F, tc::BM) ||
+  if (!tc::make_map_bf16(&xa, xn, (uint64_t)N, (uint64_t)D, tc::A_BOX) ||
+      !tc::make_map_bf16(&xh, hs_workspace, (uint64_t)N, (uint64_t)F, tc::A_BOX) ||
       !tc::make_map_bf16(&xd, ws_down, (uint64_t)D, (uint64_t)F, tc::BN) ||
       !tc::make_map_bf16(&xho, hs_workspace, (uint64_t)N, (uint64_t)F, 32) ||
       !tc::make_map_bf16(&xyo, shared_y, (uint64_t)N, (uint64_t)D, 32))
@@ -1265,10 +1290,10 @@ extern "C" moe_status_t moe_grouped_swiglu_shared(const void* x_perm, const int3
     return MOE_ERR_UNSUPPORTED;  // the shared gate/up pair must form one two-plane map
   bool gu = false;
   if (Mr > 0) {
-    if (!tc::make_map_bf16(&ma, x_perm, (uint64_t)Mr, (uint64_t)D, tc::BM) ||
+    if (!tc::make_map_bf16(&ma, gather ? xn : x_perm, (uint64_t)(gather ? N : Mr), (uint64_t)D, tc::A_BOX) ||
         !tc::make_map_bf16(&mg, w_gate, (uint64_t)G * F, (uint64_t)D, tc::BN / 2) ||
         !tc::make_map_bf16(&mu, w_up, (uint64_t)G * F, (uint64_t)D, tc::BN / 2) ||
-        !tc::make_map_bf16(&mh, h_workspace, (uint64_t)Mr, (uint64_t)F, tc::BM) ||
+        !tc::make_map_bf16(&mh, h_workspace, (uint64_t)Mr, (uint64_t)F, tc::A_BOX) ||
         !tc::make_map_bf16(&md, w_down, (uint64_t)G * D, (uint64_t)F, tc::BN) ||
         !tc::make_map_bf16(&mho, h_workspace, (uint64_t)Mr, (uint64_t)F, 32) ||
         !tc::make_map_bf16(&myo, y_perm, (uint64_t)Mr, (uint64_t)D, 32))
@@ -1281,10 +1306,15 @@ extern "C" moe_status_t moe_grouped_swiglu_shared(const void* x_perm, const int3
   }
   tc::ExtraGroup x1;
   x1.a = &xa; x1.b = &xgu; x1.out_map = &xho; x1.M = N; x1.out = hs_workspace; x1.b_planes = xplanes;
-  moe_status_t st = gu ? tc::launch<0>(ma, mgu, mgu, mho, offsets, G, Mr, D, F, h_workspace, status, s, nullptr, 0,
-                                       nullptr, planes, x1)
-                       : tc::launch<0>(ma, mg, mu, mho, offsets, G, Mr, D, F, h_workspace, status, s, nullptr, 0,
-                                       nullptr, 0, x1);
+  moe_status_t st;
+  if (gather && Mr > 0)  // GEMM1 gathers the routed rows through perm_token and the shared rows in order
+    st = gu ? tc::launch<2>(mgu, mgu, mgu, mho, offsets, G, Mr, D, F, h_workspace, status, s, xn, N, perm_token,
+                            planes, x1)
+            : tc::launch<2>(mg, mg, mu, mho, offsets, G, Mr, D, F, h_workspace, status, s, xn, N, perm_token, 0, x1);
+  else
+    st = gu ? tc::launch<0>(ma, mgu, mgu, mho, offsets, G, Mr, D, F, h_workspace, status, s, nullptr, 0, nullptr,
+                            planes, x1)
+            : tc::launch<0>(ma, mg, mu, mho, offsets, G, Mr, D, F, h_workspace, status, s, nullptr, 0, nullptr, 0, x1);
   if (st != MOE_OK) return st;
   tc::ExtraGroup x2;
   x2.a = &xh; x2.b = &xd; x2.out_map = &xyo; x2.M = N; x2.out = shared_y; x2.b_planes = 0;
@@ -1310,9 +1340,10 @@ extern "C" moe_status_t moe_grouped_swiglu_gather(const void* xn, int N, const i
   if (!status) return MOE_ERR_CUDA;
   cudaStream_t s = as_cuda(stream);
   CUtensorMap mg, mu, mh, md, mho, myo;
+  const bool pair2 = tc::use_pair(G, M_total);  // GEMM2 on CTA pairs (128-row H boxes) or one CTA
   if (!tc::make_map_bf16(&mg, w_gate, (uint64_t)G * F, (uint64_t)D, tc::BN / 2) ||
       !tc::make_map_bf16(&mu, w_up, (uint64_t)G * F, (uint64_t)D, tc::BN / 2) ||
-      !tc::make_map_bf16(&mh, h_workspace, (uint64_t)M_total, (uint64_t)F, tc::BM) ||
+      !tc::make_map_bf16(&mh, h_workspace, (uint64_t)M_total, (uint64_t)F, pair2 ? tc::BM : tc::A_BOX) ||
       !tc::make_map_bf16(&md, w_down, (uint64_t)G * D, (uint64_t)F, tc::BN) ||
       !tc::make_map_bf16(&mho, h_workspace, (uint64_t)M_total, (uint64_t)F, 32) ||
       !tc::make_map_bf16(&myo, y_perm, (uint64_t)M_total, (uint64_t)D, 32))
@@ -1325,7 +1356,7 @@ extern "C" moe_status_t moe_grouped_swiglu_gather(const void* xn, int N, const i
                        : tc::launch<2>(mg, mg, mu, mho, offsets, G, M_total, D, F, h_workspace, status, s, xn, N,
                                        perm_token);
   if (st != MOE_OK) return st;
-  if (tc::use_pair(G, M_total)) {  // GEMM2 reads H, not gathered rows: CTA pairs as in moe_grouped_swiglu
+  if (pair2) {  // GEMM2 reads H, not gathered rows: CTA pairs as in moe_grouped_swiglu
     CUtensorMap mh2, mdp;
     if (!tc::make_map_bf16(&mh2, h_workspace, (uint64_t)M_total, (uint64_t)F, tc::BM / 2) ||
         !tc::make_map_bf16(&mdp, w_down, (uint64_t)G * D, (uint64_t)F, tc::pair::HB))

@@ -71,8 +71,8 @@ def load():
         "moe_selftest_bounded_wait": ([vp, ctypes.c_longlong, vp, vp], i32),
         "moe_permute_update_bias": ([vp, i32, i32, i32, vp, i32, i32, i32, vp, vp, vp, vp, vp, vp, sz, f32, vp,
                                      vp, vp], i32),
-        "moe_grouped_swiglu_shared": ([vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp,
-                                       vp], i32),
+        "moe_grouped_swiglu_shared": ([vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp,
+                                       vp, vp], i32),
     }
     for name, (args, res) in sig.items():
         f = getattr(L, name)
@@ -341,21 +341,26 @@ def moe_grouped_swiglu(x_perm, offsets, w_gate, w_up, w_down, h_workspace=None, 
 
 
 def moe_grouped_swiglu_shared(x_perm, offsets, w_gate, w_up, w_down, xn, shared, h_workspace=None, y_perm=None,
-                              hs_workspace=None, shared_y=None, stream=None):
+                              hs_workspace=None, shared_y=None, stream=None, perm_token=None):
     """The routed experts' SwiGLU and the always-on shared expert's (shared = (w_gate[1,F,D],
-    w_up[1,F,D], w_down[1,D,F]) on xn) in the same two launches (bf16).  Returns (y_perm, shared_y)."""
+    w_up[1,F,D], w_down[1,D,F]) on xn) in the same two launches (bf16).  With perm_token the
+    routed rows are gathered from xn[perm_token] and x_perm may be None.  Returns
+    (y_perm, shared_y)."""
     L = load()
-    M, D = x_perm.shape
-    G, F, _ = w_gate.shape
+    G, F, D = w_gate.shape
+    M = perm_token.shape[0] if perm_token is not None else x_perm.shape[0]
     N = xn.shape[0]
-    dt, dev = x_perm.dtype, x_perm.device
+    dt, dev = xn.dtype, xn.device
     sg, su, sd = shared
-    _need("x_perm", x_perm, torch.bfloat16)
+    _need("xn", xn, torch.bfloat16, (N, D))
+    if perm_token is None and x_perm is None:
+        raise ValueError("x_perm or perm_token is needed")
+    _need("x_perm", x_perm, dt, (M, D), dev)
+    _need("perm_token", perm_token, torch.int32, (M,), dev)
     _need("offsets", offsets, torch.int32, (G + 1,), dev)
     _need("w_gate", w_gate, dt, (G, F, D), dev)
     _need("w_up", w_up, dt, (G, F, D), dev)
     _need("w_down", w_down, dt, (G, D, F), dev)
-    _need("xn", xn, dt, (N, D), dev)
     _need("shared w_gate", sg, dt, (1, F, D), dev)
     _need("shared w_up", su, dt, (1, F, D), dev)
     _need("shared w_down", sd, dt, (1, D, F), dev)
@@ -368,10 +373,11 @@ def moe_grouped_swiglu_shared(x_perm, offsets, w_gate, w_up, w_down, xn, shared,
     y_perm = e(M, D) if y_perm is None else y_perm
     hs_workspace = e(N, F) if hs_workspace is None else hs_workspace
     shared_y = e(N, D) if shared_y is None else shared_y
-    _cuda(x_perm, offsets, w_gate, w_up, w_down, xn, sg, su, sd, h_workspace, y_perm, hs_workspace, shared_y)
+    _cuda(x_perm, perm_token, offsets, w_gate, w_up, w_down, xn, sg, su, sd, h_workspace, y_perm, hs_workspace,
+          shared_y)
     _chk("moe_grouped_swiglu_shared", L.moe_grouped_swiglu_shared(
-        _p(x_perm), _p(offsets), G, M, D, F, _p(w_gate), _p(w_up), _p(w_down), _p(h_workspace), _p(y_perm),
-        _p(xn), N, _p(sg), _p(su), _p(sd), _p(hs_workspace), _p(shared_y), _stream(stream)))
+        _p(x_perm), _p(perm_token), _p(offsets), G, M, D, F, _p(w_gate), _p(w_up), _p(w_down), _p(h_workspace),
+        _p(y_perm), _p(xn), N, _p(sg), _p(su), _p(sd), _p(hs_workspace), _p(shared_y), _stream(stream)))
     return y_perm, shared_y
 
 
@@ -516,10 +522,9 @@ class MoELayer:
             self.sh_y = e(N, self.D, dt=dtype)
         else:
             self.sh_y = None
-        # the shared expert's tiles ride in the routed experts' launches (same d_ff, bf16, the
-        # routed rows read from x_perm)
+        # the shared expert's tiles ride in the routed experts' launches (same d_ff, bf16)
         self.fuse_shared = bool(fuse_shared) and w.shared is not None and dtype == torch.bfloat16 \
-            and not self.gather and w.shared[0].shape[1] == self.F
+            and w.shared[0].shape[1] == self.F
 
     def forward(self, xn, h, update_bias=True, stream=None, out=None):
         """out = h + shared(xn) + sum_j gate_j Expert_j(xn), and the +-gamma bias step on
@@ -567,7 +572,8 @@ class MoELayer:
         w = self.w
         if self.fuse_shared:
             moe_grouped_swiglu_shared(self.x_perm, self.offsets, w.w_gate, w.w_up, w.w_down, xn, w.shared,
-                                      self.h_ws, self.y_perm, self.sh_h, self.sh_y, stream=stream)
+                                      self.h_ws, self.y_perm, self.sh_h, self.sh_y, stream=stream,
+                                      perm_token=self.perm_token if self.gather else None)
         elif self.gather:
             moe_grouped_swiglu_gather(xn, self.perm_token, self.offsets, w.w_gate, w.w_up,
                                       w.w_down, self.h_ws, self.y_perm, stream=stream)

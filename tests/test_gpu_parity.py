@@ -370,13 +370,15 @@ def test_permute_update_bias_matches_separate_calls(N, E, k, cap):
     assert np.array_equal(b_got.cpu().numpy(), want) and abs(mom_got.item() - mm) <= 1e-6 * mm
 
 
+@pytest.mark.parametrize("gather", [False, True], ids=["copy", "gather"])
 @pytest.mark.parametrize("N,D,E,F,k", [(1000, 256, 32, 128, 4), (300, 512, 16, 256, 2), (2048, 256, 4, 128, 2),
                                        (4096, 7168, 256, 2048, 8)],
                          ids=["small", "ragged", "pair-routed-then-shared-alone", "deepseek_v3"])
-def test_shared_expert_in_routed_launches(N, D, E, F, k):
+def test_shared_expert_in_routed_launches(N, D, E, F, k, gather):
     """moe_grouped_swiglu_shared (the shared expert's tiles after the routed experts' tiles in
-    the same two launches) gives the same bits as the routed call followed by the shared
-    expert's own call, and the oracle's shared expert within the bf16 tolerance."""
+    the same two launches), with the routed rows read from x_perm or gathered from xn through
+    perm_token, gives the same bits as the routed call followed by the shared expert's own
+    call, and the oracle's shared expert within the bf16 tolerance."""
     cfg = synth.scaled(synth.CONFIGS["deepseek_v3"], N=N, D=D, E=E, F=F, k=k, F_shared=F)
     xn, _ = synth.make_tokens(cfg, "cuda")
     wg, wu, wd = synth.make_experts(cfg, "cuda")
@@ -387,7 +389,10 @@ def test_shared_expert_in_routed_launches(N, D, E, F, k):
     y_ref = moe.moe_grouped_swiglu(x_perm, offsets, wg, wu, wd)
     off_sh = torch.tensor([0, N], dtype=torch.int32, device="cuda")
     sh_ref = moe.moe_grouped_swiglu(xn, off_sh, *sh)
-    y, sh_y = moe.moe_grouped_swiglu_shared(x_perm, offsets, wg, wu, wd, xn, sh)
+    if gather:
+        y, sh_y = moe.moe_grouped_swiglu_shared(None, offsets, wg, wu, wd, xn, sh, perm_token=perm)
+    else:
+        y, sh_y = moe.moe_grouped_swiglu_shared(x_perm, offsets, wg, wu, wd, xn, sh)
     torch.cuda.synchronize()
     assert moe.last_device_status() == 0
     assert torch.equal(y, y_ref) and torch.equal(sh_y, sh_ref)
