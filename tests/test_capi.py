@@ -69,15 +69,12 @@ def test_new_entry_points_reject_bad_arguments_before_launch(lib):
     g.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                   ctypes.c_int] + [ctypes.c_void_p] * 5 + [ctypes.c_void_p, ctypes.c_int] + [ctypes.c_void_p] * 6
     g.restype = ctypes.c_int
-    tok = ctypes.c_void_p(16)  # never dereferenced: every call below is rejected on the host
     assert g(None, None, None, 0, 0, 128, 128, None, None, None, None, None, None, 0, None, None, None, None, None,
              None) == -1                                            # G < 1
     assert g(None, None, None, 4, 0, 100, 128, None, None, None, None, None, None, 0, None, None, None, None, None,
              None) == -2                                            # D not a multiple of 64
     assert g(None, None, None, 4, 64, 128, 128, None, None, None, None, None, None, 0, None, None, None, None, None,
              None) == -1                                            # routed rows but no operands
-    assert g(None, tok, None, 4, 64, 128, 128, None, None, None, None, None, None, 0, None, None, None, None, None,
-             None) == -1                                            # rows to gather, no tokens
     assert g(None, None, None, 4, 0, 128, 128, None, None, None, None, None, None, 8, None, None, None, None, None,
              None) == -1                                            # shared rows but no operands
 
