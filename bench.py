@@ -102,6 +102,22 @@ def config_dict(cfg, k, world):
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
 
 
+def router_bound(alg, us, pk, tensor_cores):
+    """The router's roofline time and its fraction of the measured time: the slower of its
+    bytes at the measured HBM bandwidth and its multiply-adds at the peak of the unit that runs
+    them -- on tensor cores three bf16 products per fp32 weight (the exact three-plane split),
+    on CUDA cores one fp32 FMA each."""
+    t_bytes = alg["router_bytes"] / (pk["hbm_gbs"] * 1e9)
+    if tensor_cores:
+        flops, peak, unit = 3.0 * alg["router_flops"], pk["bf16_tflops"] * 1e12, "bf16 tensor (burst), 3 planes"
+    else:
+        flops, peak, unit = alg["router_flops"], F32_ALU_TFLOPS * 1e12, "fp32 FMA"
+    t_flops = flops / peak
+    bound = max(t_bytes, t_flops)
+    return {"bound": "tensor" if t_flops > t_bytes else "hbm", "bound_us": round(bound * 1e6, 2),
+            "bound_time_frac": bound / (us * 1e-6), "compute": unit}
+
+
 def algorithmic(cfg, k=None, copy_rows=False):
     """Algorithmic flops and bytes of each step (only what the method must move).  The
     permute moves token rows only when the first GEMM does not gather them itself."""
@@ -523,9 +539,10 @@ def measure(wl, steps, warmup, world, pk, e2e_steps):
                              tflops=alg["gemm_flops"] / (stage_us["grouped_swiglu"] * 1e-6) / 1e12,
                              algorithmic_gflop=alg["gemm_flops"] / 1e9,
                              algorithmic_gb=alg["gemm_bytes"] / 1e9),
-        "router": {"gbs": gbs(alg["router_bytes"], stage_us["router"]),
-                   "frac_hbm": gbs(alg["router_bytes"], stage_us["router"]) / hbm,
-                   "algorithmic_mb": alg["router_bytes"] / 1e6, "launches": 3 if L.tc_router else 1},
+        "router": dict({"gbs": gbs(alg["router_bytes"], stage_us["router"]),
+                        "frac_hbm": gbs(alg["router_bytes"], stage_us["router"]) / hbm,
+                        "algorithmic_mb": alg["router_bytes"] / 1e6, "launches": 3 if L.tc_router else 1},
+                       **router_bound(alg, stage_us["router"], pk, L.tc_router)),
         "permute": {"moves_rows": not L.gather, "us": round(stage_us["permute"], 2),
                     "gbs": gbs(alg["permute_bytes"], stage_us["permute"]) if not L.gather else None,
                     "frac_hbm": gbs(alg["permute_bytes"], stage_us["permute"]) / hbm if not L.gather else None,

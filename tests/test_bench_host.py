@@ -118,3 +118,20 @@ def test_clock_summary_keeps_the_timed_window(tmp_path):
         f.write("\n".join(rows) + "\n")
     d = s.summary((w0 + 0.101, w0 + 0.102))
     assert d["scope"].startswith("nearest") and d["samples"] == 3
+
+
+def test_router_bound_takes_the_slower_of_bytes_and_split_products():
+    """The router's roofline time: DeepSeek-V3 shape on tensor cores is bound by its three
+    bf16 products per weight (3 * 2 N D E flops), the fp32 CUDA-core router by its bytes."""
+    pk = {"hbm_gbs": 6425.0, "bf16_tflops": 1808.6}
+    cfg = synth.CONFIGS["deepseek_v3"]
+    alg = bench.algorithmic(cfg)
+    r = bench.router_bound(alg, 100.0, pk, True)
+    t_flops = 3 * 2.0 * cfg.N * cfg.D * cfg.E / 1808.6e12
+    assert r["bound"] == "tensor" and abs(r["bound_us"] - t_flops * 1e6) < 0.01
+    assert abs(r["bound_time_frac"] - t_flops / 100e-6) < 1e-9
+    tiny = synth.CONFIGS["tiny"]
+    a2 = bench.algorithmic(tiny)
+    r2 = bench.router_bound(a2, 10.0, pk, False)
+    t_bytes = a2["router_bytes"] / 6425e9
+    assert r2["bound"] == "hbm" and abs(r2["bound_us"] - round(t_bytes * 1e6, 2)) < 1e-9
