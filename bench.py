@@ -233,6 +233,75 @@ def clock_problem(summary):
     return None
 
 
+def sustained_gemm(wl, calls=20, reps=25):
+    """The layer's expert call (the grouped SwiGLU, with the shared expert's tiles when the
+    layer runs them there) in a sustained loop -- a CUDA graph of `calls` back-to-back calls,
+    replayed `reps` times (about 2 s on the DeepSeek-V3 layer) -- on three inputs that move the
+    same bytes: the layer's routed counts, perfectly balanced counts (N k / E rows per expert:
+    no padded row tiles) and all-zero activations with the routed counts.  With the power draw
+    and SM clock that nvidia-smi reports over each loop: where the GPU holds its power limit,
+    the differences show what the call's speed follows there."""
+    L, cfg = wl.layer, wl.cfg
+    wl.run()  # one forward: counts, offsets, permuted rows
+    torch.cuda.synchronize()
+    real = L.offsets.clone()
+    R = cfg.N * wl.k
+    balanced = torch.arange(0, R + 1, R // cfg.E, dtype=torch.int32, device=real.device) \
+        if R % cfg.E == 0 else None
+    zeros = torch.zeros_like(wl.xn)
+
+    def tiles(off):
+        c = (off[1:] - off[:-1]).long()
+        return {"row_tiles": int(((c + 127) // 128).sum()), "half_tiles": int(((c % 128 > 0) & (c % 128 <= 64)).sum())}
+
+    out = {}
+    for name, off, xs, zero in (("routed counts", real, wl.xn, False), ("balanced counts", balanced, wl.xn, False),
+                                ("zero activations", real, zeros, True)):
+        if off is None:
+            continue
+        L.offsets.copy_(off)
+        saved = None
+        if zero and L.x_perm is not None:
+            saved = L.x_perm.clone()
+            L.x_perm.zero_()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+
+        def call():
+            L.experts(xs, stream=s)
+            L.shared_expert(xs, stream=s)
+        with torch.cuda.stream(s):
+            call()
+        s.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for _ in range(calls):
+                call()
+        torch.cuda.current_stream().wait_stream(s)
+        g.replay()
+        g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with ClockSampler(torch.cuda.current_device()) as clk:
+            t0 = time.time()
+            e0.record()
+            for _ in range(reps):
+                g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            t1 = time.time()
+        st = moe.last_device_status()
+        if st != 0:
+            raise SystemExit(f"device status {moe.STATUS.get(st, st)} in the sustained loop ({name})")
+        out[name] = dict(tiles(off), ms_per_call=e0.elapsed_time(e1) / (calls * reps), clocks=clk.summary((t0, t1)))
+        del g
+        if saved is not None:
+            L.x_perm.copy_(saved)
+        time.sleep(1.0)
+    L.offsets.copy_(real)
+    return out
+
+
 def cpu_model():
     try:
         with open("/proc/cpuinfo") as f:
@@ -712,6 +781,9 @@ def main():
                       help="the permute writes the permuted rows x_perm and GEMM1 loads them by TMA")
     ap.add_argument("--shared-separate", action="store_true",
                     help="run the shared expert in launches of its own instead of inside the routed experts' launches")
+    ap.add_argument("--sustained-gemm", action="store_true",
+                    help="print only the expert call timed in a sustained loop on routed counts, "
+                         "balanced counts and zero activations, with power and SM clock")
     rows.add_argument("--gather", action="store_true",
                       help="GEMM1 gathers its rows from xn through perm_token (default: the layer "
                            "chooses by size)")
@@ -739,6 +811,11 @@ def main():
 
     wl = Workload(cfg, k, dev, rank, world, gather=gather, fuse_shared=not args.shared_separate)
     torch.cuda.synchronize()
+    if args.sustained_gemm:
+        if rank == 0:
+            print(json.dumps({"sustained_gemm": sustained_gemm(wl), "config": config_dict(cfg, k, world),
+                              "gemm1_rows": "gathered from xn" if wl.layer.gather else "permuted copy x_perm"}))
+        return
     with ClockSampler(local) as clk:
         head, total_ms = measure(wl, args.steps, args.warmup, world, pk, args.e2e_steps)
     clocks = clk.summary(head.pop("timed_window"))

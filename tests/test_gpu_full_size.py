@@ -163,3 +163,22 @@ def test_generator_bits_equal_on_gpu_and_cpu():
             a = synth.gaussian_at(cfg.seed, stream, idx.cuda(), 0.1, torch.bfloat16).cpu()
             b = synth.gaussian_at(cfg.seed, stream, idx, 0.1, torch.bfloat16)
             assert torch.equal(a, b)
+
+
+def test_sustained_gemm_mode_runs_its_three_inputs():
+    """bench.py --sustained-gemm on a small layer: three loops, the same bits as before for the
+    layer afterwards (the mode restores the offsets and the permuted rows it changes)."""
+    import bench
+    cfg = synth.scaled(synth.CONFIGS["deepseek_v3"], N=512, D=256, E=32, F=128, k=8, F_shared=128)
+    wl = bench.Workload(cfg, cfg.k, torch.device("cuda"))
+    b0 = wl.layer.w.bias.clone()  # every forward steps the bias: each run below starts from b0
+    out0 = wl.run().clone()
+    r = bench.sustained_gemm(wl, calls=2, reps=2)
+    assert set(r) == {"routed counts", "balanced counts", "zero activations"}
+    assert r["balanced counts"]["row_tiles"] == cfg.E and r["balanced counts"]["half_tiles"] == 0
+    assert all(v["ms_per_call"] > 0 for v in r.values())
+    wl.layer.w.bias.copy_(b0)
+    out1 = wl.run()
+    torch.cuda.synchronize()
+    assert moe.last_device_status() == 0
+    assert torch.equal(out0, out1)
