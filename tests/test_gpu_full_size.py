@@ -24,11 +24,14 @@ from tests import parity as P
 
 pytestmark = pytest.mark.gpu
 
-CASES = [("handbook", None), ("mixtral", None), ("deepseek_v3", None), ("skewed", 8), ("skewed", 4)]
+# (config, k, gather): gather None is the layer's own choice; the DeepSeek-V3 layer also runs
+# with its routed rows gathered (the shared expert's tiles then ride in the gathering launch)
+CASES = [("handbook", None, None), ("mixtral", None, None), ("deepseek_v3", None, None),
+         ("deepseek_v3", None, True), ("skewed", 8, None), ("skewed", 4, None)]
 SAMPLE = 6
 
 
-def _layer(cfg, k):
+def _layer(cfg, k, gather=None):
     dev = "cuda"
     xn, h = synth.make_tokens(cfg, dev)
     w_r, b = synth.make_router(cfg, dev)
@@ -36,18 +39,21 @@ def _layer(cfg, k):
     wg, wu, wd = synth.make_experts(cfg, dev)
     sh = synth.make_shared(cfg, dev)
     b0 = b.clone()
-    layer = moe.MoELayer(moe.LayerWeights(w_r, b, wg, wu, wd, sh), cfg.N, k, cfg.score_fn, cfg.gamma)
+    layer = moe.MoELayer(moe.LayerWeights(w_r, b, wg, wu, wd, sh), cfg.N, k, cfg.score_fn, cfg.gamma,
+                         gather=gather)
+    assert gather is None or layer.gather == gather
     out = layer.forward(xn, h)
     torch.cuda.synchronize()
     assert moe.last_device_status() == 0
     return layer, xn, h, b0, out
 
 
-@pytest.mark.parametrize("name,k", CASES, ids=[f"{n}-k{k or synth.CONFIGS[n].k}" for n, k in CASES])
-def test_full_size_layer(name, k):
+@pytest.mark.parametrize("name,k,gather", CASES,
+                         ids=[f"{n}-k{k or synth.CONFIGS[n].k}" + ("-gather" if g else "") for n, k, g in CASES])
+def test_full_size_layer(name, k, gather):
     cfg = synth.CONFIGS[name]
     k = cfg.k if k is None else k
-    layer, xn, h, b0, out = _layer(cfg, k)
+    layer, xn, h, b0, out = _layer(cfg, k, gather)
 
     # --- routing, every token -------------------------------------------------------
     xc, hc = synth.make_tokens(cfg, "cpu")
