@@ -123,6 +123,34 @@ def test_routing_replay_and_bad_ids():
     assert moe.last_device_status() == 0  # reading clears it
 
 
+@pytest.mark.parametrize("N,k,E,cap", [(2049, 8, 64, None), (2049, 8, 256, 40), (16384, 1, 8, 1500),
+                                       (1, 4, 16, None), (700, 3, 300, None)],
+                         ids=["16392-slots", "16392-slots-cap", "k1-cap", "one-token", "E300"])
+def test_permute_skewed_ids(N, k, E, cap):
+    """Caller-supplied ids drawn with Zipf-like popularity, so that popular experts overflow a
+    capacity: counts, offsets, row map and permutation equal the oracle's bit for bit (dropped
+    slots row -1), and the copied rows are the oracle's rows."""
+    rng = np.random.default_rng(N * 7 + E)
+    pop = 1.0 / np.arange(1, E + 1) ** 0.8
+    pop /= pop.sum()
+    idx = np.stack([rng.choice(E, k, replace=False, p=pop) for _ in range(N)]).astype(np.int32)
+    cfg = synth.scaled(C["handbook"], N=N, D=64, E=E, F=64, k=k)
+    xn, _ = synth.make_tokens(cfg, "cuda")
+    counts, offsets, row_map, perm, x_perm = moe.moe_permute(xn, torch.from_numpy(idx).cuda(), E, capacity=cap)
+    torch.cuda.synchronize()
+    assert moe.last_device_status() == 0
+    oc = moe_oracle.expert_counts(idx, E)
+    oo = moe_oracle.exclusive_scan(oc if cap is None else np.minimum(oc, cap))
+    orm, opt = moe_oracle.stable_permutation(idx, oo, capacity=cap)
+    if cap is not None:
+        assert (orm < 0).any()  # some slots dropped
+    kept = int(oo[-1])
+    assert np.array_equal(counts.cpu().numpy(), oc) and np.array_equal(offsets.cpu().numpy(), oo)
+    assert np.array_equal(row_map.cpu().numpy(), orm)
+    assert np.array_equal(perm[:kept].cpu().numpy(), opt)
+    assert torch.equal(x_perm[:kept].cpu(), synth.make_tokens(cfg)[0][torch.from_numpy(opt)])
+
+
 def test_empty_batch_is_a_no_op():
     cfg = synth.scaled(C["handbook"], N=0, D=128, E=8, F=128, k=2)
     w = torch.zeros(8, 128, device="cuda")
