@@ -86,3 +86,20 @@ def test_nonfinite_logits_are_reported(path):
         assert len(set(ids)) == cfg.k and all(0 <= e < cfg.E for e in ids)
     _, idx, _, _ = run(xn)                              # clean input: clean status again
     assert moe.last_device_status() == 0 and torch.equal(idx, idx0)
+
+
+def test_shared_call_rejects_rows_to_gather_without_tokens():
+    """moe_grouped_swiglu_shared asked to gather routed rows (perm_token given) from N = 0 tokens
+    returns MOE_ERR_INVALID_ARG on the host: nothing is launched, nothing is read."""
+    G, D, F, M = 4, 128, 128, 64
+    z = lambda *sh: torch.zeros(*sh, dtype=torch.bfloat16, device="cuda")
+    wg, wu, wd = z(G, F, D), z(G, F, D), z(G, D, F)
+    offsets = torch.tensor([0, 16, 32, 48, 64], dtype=torch.int32, device="cuda")
+    perm = torch.zeros(M, dtype=torch.int32, device="cuda")
+    h, y, xn = z(M, F), z(M, D), z(8, D)
+    L = moe.load()
+    p = moe._p
+    assert L.moe_grouped_swiglu_shared(None, p(perm), p(offsets), G, M, D, F, p(wg), p(wu), p(wd), p(h), p(y), p(xn),
+                                       0, None, None, None, None, None, moe._stream()) == -1
+    torch.cuda.synchronize()
+    assert moe.last_device_status() == 0
