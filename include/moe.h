@@ -290,7 +290,8 @@ moe_status_t moe_permute_noalloc(const void* xn, moe_dtype_t dtype, int N, int D
  * MOE_BF16: tcgen05 tensor-core kernels, fp32 accumulation in tensor memory, H and Y
  *           rounded to bf16.  When the groups average at least 256 rows, two-CTA
  *           clusters share each 256-row tile (tcgen05 cta_group::2); otherwise one CTA
- *           per 128-row tile.  Both give the same bits.  The environment variable
+ *           per 128-row tile (M = 64 MMAs for a group's last <= 64 rows).  Both give the
+ *           same bits.  The environment variable
  *           MOE_GROUPED_GEMM=pair or =single forces one of the two (read on every call).
  *           MOE_F32: CUDA-core fp32 kernels.
  * Requires D % 64 == 0, F % 64 == 0, 1 <= G.
@@ -317,7 +318,7 @@ moe_status_t moe_grouped_swiglu_ex(const void* x_perm, moe_dtype_t dtype, const 
  * moe_grouped_swiglu_shared -- the routed experts' SwiGLU FFNs and the always-on shared
  * expert's, in the same two launches.  Lesson "Shared experts" (one expert every token
  * visits, added to the routed sum) and "Concept" (every expert a SwiGLU FFN).  The shared
- * expert's 128-row tiles follow the routed experts' tiles in each launch's tile list, so it
+ * expert's row tiles follow the routed experts' tiles in each launch's tile list, so it
  * needs no launches of its own and fills the routed tiles' last wave.  Same bits as
  * moe_grouped_swiglu (or moe_grouped_swiglu_gather) on the routed rows followed by
  * moe_grouped_swiglu with G = 1, offsets {0, N} on xn.
