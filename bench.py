@@ -323,7 +323,7 @@ class Workload:
     # "bias": the separate bias step of replicas (empty on one GPU, where the permute does it)
     STAGES = ("router", "permute", "grouped_swiglu", "shared", "combine", "bias")
 
-    def __init__(self, cfg, k, dev, rank=0, world=1, gather=None, fuse_shared=True):
+    def __init__(self, cfg, k, dev, rank=0, world=1, gather=None, fuse_shared=True, router_shared=False):
         self.cfg, self.k, self.dev, self.world = cfg, k, dev, world
         self.xn, self.h = synth.make_tokens(cfg, dev, seed=cfg.seed + 1000 * rank)
         w_r, b = synth.make_router(cfg, dev)
@@ -331,7 +331,8 @@ class Workload:
         sh = synth.make_shared(cfg, dev)
         dt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
         self.layer = moe.MoELayer(moe.LayerWeights(w_r, b, wg, wu, wd, sh), cfg.N, k, cfg.score_fn,
-                                  cfg.gamma, dtype=dt, gather=gather, fuse_shared=fuse_shared)
+                                  cfg.gamma, dtype=dt, gather=gather, fuse_shared=fuse_shared,
+                                  router_shared=router_shared)
 
     def run(self, xn=None, h=None, events=None, out=None):
         L = self.layer
@@ -582,9 +583,13 @@ def measure(wl, steps, warmup, world, pk, e2e_steps):
             return max(flops / (pt * 1e12), bytes_ / (pk["hbm_gbs"] * 1e9))
         t_phases = bound_s(a["gemm_flops"], a["gemm_bytes"])
         if L.fuse_shared:  # the shared expert's tiles run in the routed experts' launches, after theirs
-            t_phases += bound_s(a["shared_flops"], a["shared_bytes"])
-            a["gemm_flops"] += a["shared_flops"]
-            a["gemm_bytes"] += a["shared_bytes"]
+            sf, sb = a["shared_flops"], a["shared_bytes"]
+            if L.router_shared:  # only its second GEMM: W_down, H read, output written
+                Fs = cfg.F_shared
+                sf, sb = sf / 3.0, (cfg.D * Fs + cfg.N * Fs + cfg.N * cfg.D) * 2.0
+            t_phases += bound_s(sf, sb)
+            a["gemm_flops"] += sf
+            a["gemm_bytes"] += sb
         r = roofline_of(a["gemm_flops"], a["gemm_bytes"], stage_us["grouped_swiglu"], pk, sustained, cfg.dtype)
         if L.fuse_shared and cfg.dtype == "bf16":
             r["bound_time_frac"] = t_phases / (stage_us["grouped_swiglu"] * 1e-6)
@@ -602,7 +607,9 @@ def measure(wl, steps, warmup, world, pk, e2e_steps):
         "stage_us": {n: round(v, 2) for n, v in stage_us.items()},
         "stage_sum_us": round(sum(stage_us.values()), 2), "stage_us_from": how,
         "_gemm_sustained": gemm_roofline(True)[0],
-        "grouped_gemm": dict(gemm, kernel="moe_grouped_swiglu_shared (routed + shared expert)" if L.fuse_shared
+        "grouped_gemm": dict(gemm, kernel="moe_grouped_swiglu_shared_h (routed + the shared expert's GEMM2; its "
+                             "GEMM1 in the router launch)" if L.router_shared
+                             else "moe_grouped_swiglu_shared (routed + shared expert)" if L.fuse_shared
                              else ("moe_grouped_swiglu_gather" if L.gather else "moe_grouped_swiglu"),
                              launches="GEMM1+SwiGLU and GEMM2", us=round(stage_us["grouped_swiglu"], 2),
                              tflops=alg["gemm_flops"] / (stage_us["grouped_swiglu"] * 1e-6) / 1e12,
@@ -781,6 +788,8 @@ def main():
                       help="the permute writes the permuted rows x_perm and GEMM1 loads them by TMA")
     ap.add_argument("--shared-separate", action="store_true",
                     help="run the shared expert in launches of its own instead of inside the routed experts' launches")
+    ap.add_argument("--router-shared", action="store_true",
+                    help="the shared expert's first GEMM in the router's launch (moe_router_topk_split_shared)")
     ap.add_argument("--sustained-gemm", action="store_true",
                     help="print only the expert call timed in a sustained loop on routed counts, "
                          "balanced counts and zero activations, with power and SM clock")
@@ -809,7 +818,8 @@ def main():
     pk, pk_kind = peaks()
     gather = True if args.gather else (False if args.permute_copy else None)
 
-    wl = Workload(cfg, k, dev, rank, world, gather=gather, fuse_shared=not args.shared_separate)
+    wl = Workload(cfg, k, dev, rank, world, gather=gather, fuse_shared=not args.shared_separate,
+                  router_shared=args.router_shared)
     torch.cuda.synchronize()
     if args.sustained_gemm:
         if rank == 0:
@@ -836,7 +846,9 @@ def main():
     roof = {k2: g[k2] for k2 in ("bound", "achieved", "peak", "unit", "frac", "peak_kind", "peak_reason",
                                  "frac_of_burst", "bound_time_frac", "bound_time_note") if k2 in g}
     roof.update({"kernel": f"{g['kernel']} ({g['launches']} launches, one call)",
-                 "traffic": recorded_traffic(cfg, wl.layer.gather), "traffic_unit": "bytes per call (ncu)",
+                 # the record is the default call's (with the shared expert's first GEMM)
+                 "traffic": None if wl.layer.router_shared else recorded_traffic(cfg, wl.layer.gather),
+                 "traffic_unit": "bytes per call (ncu)",
                  "peak_source": pk_kind, "timed": head["stage_us_from"],
                  "algorithmic": (f"{g['algorithmic_gb']:.2f} GB" if g["bound"] == "hbm"
                                  else f"{g['algorithmic_gflop']:.1f} GFLOP") + " per call",

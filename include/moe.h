@@ -152,11 +152,11 @@ moe_status_t moe_router_split(const float* w_router, int E, int D, void* w_split
 /*
  * moe_router_topk_split -- moe_router_topk on tensor cores, for bf16 activations.
  * Same router as moe_router_topk (lesson "Build it" step 1; the handbook article's fp32
- * router): logits = xn . (hi + mid + lo)^T, every bf16 x bf16 product exact.  The hi plane
- * is summed per 64-element slice of D in a fresh fp32 TMEM accumulator and the slice
- * partials are added in fp32 with two-sum compensation; the mid and lo planes (2^-8 and
- * 2^-16 of the weight) accumulate over all of D on the tensor cores.  Short batches split
- * D across CTAs; their partial logits go to `workspace` and are added in split order.
+ * router): logits = xn . (hi + mid + lo)^T, every bf16 x bf16 product exact.  The three
+ * planes' products are summed per 64-element slice of D in a fresh fp32 TMEM accumulator;
+ * the slice partials hi + (mid + lo) are added in fp32 and folded into a two-sum
+ * compensated total every 8 slices.  Short batches split D across CTAs; their partial
+ * logits go to `workspace` and are added in split order.
  *   xn        [N, D] bf16
  *   w_split   [3, E, D] bf16 from moe_router_split
  *   logits_out[N, E] fp32 -- REQUIRED here (the top-k reads it back)
@@ -170,6 +170,29 @@ moe_status_t moe_router_topk_split(const void* xn, int N, int D, const void* w_s
                                    float* logits_out, int32_t* topk_idx, float* topk_gate,
                                    uint8_t* near_tie, void* workspace, size_t workspace_bytes,
                                    moe_stream_t stream);
+
+/*
+ * moe_router_topk_split_shared -- moe_router_topk_split and the shared expert's first GEMM
+ * in one launch over the same 128-token tiles of xn (the router's split weight rows and the
+ * shared expert's gate/up rows read against the same activation tiles, so xn comes from HBM
+ * once; handbook news article, why bytes moved around the expert GEMMs matter).  Lesson
+ * "Shared experts": the always-on expert's H = SiLU(xn ws_gate^T) * (xn ws_up^T).
+ *   xn .. workspace_bytes   as moe_router_topk_split (the same logits, ids, gates and flags)
+ *   ws_gate, ws_up [F, D]   bf16, the shared expert's gate and up projections; they must be
+ *                           addressable as the two planes of one tensor (distance >= F*D*2
+ *                           bytes, a multiple of 16), else MOE_ERR_UNSUPPORTED
+ *   hs_out [N, F]           bf16 out: the shared expert's H, the same bits as the first GEMM of
+ *                           moe_grouped_swiglu with G = 1, offsets {0, N}
+ * Then moe_grouped_swiglu_shared_h runs its second GEMM in the routed experts' GEMM2 launch.
+ * Requires F % 64 == 0 and the conditions of moe_router_topk_split; MOE_ERR_INVALID_ARG for
+ * NULL ws_gate, ws_up or hs_out.
+ */
+moe_status_t moe_router_topk_split_shared(const void* xn, int N, int D, const void* w_split,
+                                          const float* bias, int E, int k, moe_score_fn_t fn,
+                                          float* logits_out, int32_t* topk_idx, float* topk_gate,
+                                          uint8_t* near_tie, void* workspace, size_t workspace_bytes,
+                                          const void* ws_gate, const void* ws_up, int F, void* hs_out,
+                                          moe_stream_t stream);
 
 /* Bytes of scratch moe_permute needs for (N, k, E). */
 size_t moe_permute_workspace_bytes(int N, int k, int E);
@@ -342,6 +365,19 @@ moe_status_t moe_grouped_swiglu_shared(const void* x_perm, const int32_t* perm_t
                                        const void* xn, int N, const void* ws_gate, const void* ws_up,
                                        const void* ws_down, void* hs_workspace, void* shared_y,
                                        moe_stream_t stream);
+
+/*
+ * moe_grouped_swiglu_shared_h -- moe_grouped_swiglu_shared when hs_workspace already holds
+ * the shared expert's H (from moe_router_topk_split_shared): the routed experts' two GEMMs,
+ * and the shared expert's second GEMM as extra tiles of the routed GEMM2 launch.  Same
+ * arguments minus ws_gate / ws_up; xn is read only when perm_token is given.  Same bits as
+ * moe_grouped_swiglu_shared given the same H.
+ */
+moe_status_t moe_grouped_swiglu_shared_h(const void* x_perm, const int32_t* perm_token, const int32_t* offsets,
+                                         int G, int M_total, int D, int F, const void* w_gate,
+                                         const void* w_up, const void* w_down, void* h_workspace, void* y_perm,
+                                         const void* xn, int N, const void* ws_down, void* hs_workspace,
+                                         void* shared_y, moe_stream_t stream);
 
 /*
  * moe_grouped_swiglu_gather -- moe_grouped_swiglu with the permutation folded into

@@ -1240,13 +1240,15 @@ extern "C" moe_status_t moe_grouped_swiglu_ex(const void* x_perm, moe_dtype_t dt
   return st;
 }
 
-extern "C" moe_status_t moe_grouped_swiglu_shared(const void* x_perm, const int32_t* perm_token,
-                                                  const int32_t* offsets, int G, int M_total, int D, int F,
-                                                  const void* w_gate, const void* w_up, const void* w_down,
-                                                  void* h_workspace, void* y_perm, const void* xn, int N,
-                                                  const void* ws_gate, const void* ws_up, const void* ws_down,
-                                                  void* hs_workspace, void* shared_y, moe_stream_t stream) {
-  using namespace moe;
+namespace moe {
+namespace {
+// moe_grouped_swiglu_shared; with h_ready, hs_workspace already holds the shared expert's H
+// (made by the router launch) and only its second GEMM runs, in the routed GEMM2 launch.
+moe_status_t grouped_shared_impl(const void* x_perm, const int32_t* perm_token, const int32_t* offsets, int G,
+                                 int M_total, int D, int F, const void* w_gate, const void* w_up,
+                                 const void* w_down, void* h_workspace, void* y_perm, const void* xn, int N,
+                                 const void* ws_gate, const void* ws_up, const void* ws_down, void* hs_workspace,
+                                 void* shared_y, moe_stream_t stream, bool h_ready) {
   const bool gather = perm_token != nullptr;  // routed rows read from xn through perm_token
   if (G < 1 || M_total < 0 || D <= 0 || F <= 0 || N < 0) return MOE_ERR_INVALID_ARG;
   if (D % 64 != 0 || F % 64 != 0 || G > tc::MAX_GROUPS) return MOE_ERR_UNSUPPORTED;
@@ -1254,7 +1256,8 @@ extern "C" moe_status_t moe_grouped_swiglu_shared(const void* x_perm, const int3
   if (M_total > 0 && ((!gather && !x_perm) || !offsets || !w_gate || !w_up || !w_down || !h_workspace || !y_perm))
     return MOE_ERR_INVALID_ARG;
   if (gather && M_total > 0 && (!xn || N < 1)) return MOE_ERR_INVALID_ARG;
-  if (N > 0 && (!xn || !ws_gate || !ws_up || !ws_down || !hs_workspace || !shared_y)) return MOE_ERR_INVALID_ARG;
+  if (N > 0 && (!ws_down || !hs_workspace || !shared_y || (!h_ready && (!xn || !ws_gate || !ws_up))))
+    return MOE_ERR_INVALID_ARG;
   for (const void* p : {x_perm, (const void*)w_gate, w_up, w_down, (const void*)h_workspace, (const void*)y_perm, xn,
                         ws_gate, ws_up, ws_down, (const void*)hs_workspace, (const void*)shared_y})
     if (p && !aligned16(p)) return MOE_ERR_INVALID_ARG;
@@ -1280,14 +1283,16 @@ extern "C" moe_status_t moe_grouped_swiglu_shared(const void* x_perm, const int3
   CUtensorMap ma, mg, mu, mh, md, mho, myo, mgu;
   CUtensorMap xa, xgu, xh, xd, xho, xyo;
   int planes = 0, xplanes = 0;
-  if (!tc::make_map_bf16(&xa, xn, (uint64_t)N, (uint64_t)D, tc::A_BOX) ||
-      !tc::make_map_bf16(&xh, hs_workspace, (uint64_t)N, (uint64_t)F, tc::A_BOX) ||
+  if (!tc::make_map_bf16(&xh, hs_workspace, (uint64_t)N, (uint64_t)F, tc::A_BOX) ||
       !tc::make_map_bf16(&xd, ws_down, (uint64_t)D, (uint64_t)F, tc::BN) ||
       !tc::make_map_bf16(&xho, hs_workspace, (uint64_t)N, (uint64_t)F, 32) ||
       !tc::make_map_bf16(&xyo, shared_y, (uint64_t)N, (uint64_t)D, 32))
     return MOE_ERR_CUDA;
-  if (!tc::make_map_gate_up(&xgu, ws_gate, ws_up, (uint64_t)F, (uint64_t)D, tc::BN / 2, &xplanes))
-    return MOE_ERR_UNSUPPORTED;  // the shared gate/up pair must form one two-plane map
+  if (!h_ready) {  // the shared expert's first GEMM runs here too
+    if (!tc::make_map_bf16(&xa, xn, (uint64_t)N, (uint64_t)D, tc::A_BOX)) return MOE_ERR_CUDA;
+    if (!tc::make_map_gate_up(&xgu, ws_gate, ws_up, (uint64_t)F, (uint64_t)D, tc::BN / 2, &xplanes))
+      return MOE_ERR_UNSUPPORTED;  // the shared gate/up pair must form one two-plane map
+  }
   bool gu = false;
   if (Mr > 0) {
     if (!tc::make_map_bf16(&ma, gather ? xn : x_perm, (uint64_t)(gather ? N : Mr), (uint64_t)D, tc::A_BOX) ||
@@ -1300,14 +1305,21 @@ extern "C" moe_status_t moe_grouped_swiglu_shared(const void* x_perm, const int3
       return MOE_ERR_CUDA;
     gu = tc::make_map_gate_up(&mgu, w_gate, w_up, (uint64_t)G * F, (uint64_t)D, tc::BN / 2, &planes);
   } else {  // no routed tiles: the shared expert's maps stand in for the unused routed ones
-    ma = xa; mgu = xgu; mg = xgu; mu = xgu; mh = xh; md = xd; mho = xho; myo = xyo;
-    gu = true;
-    planes = xplanes;
+    mh = xh; md = xd; mho = xho; myo = xyo;
+    if (!h_ready) {
+      ma = xa; mgu = xgu; mg = xgu; mu = xgu;
+      gu = true;
+      planes = xplanes;
+    }
   }
   tc::ExtraGroup x1;
-  x1.a = &xa; x1.b = &xgu; x1.out_map = &xho; x1.M = N; x1.out = hs_workspace; x1.b_planes = xplanes;
-  moe_status_t st;
-  if (gather && Mr > 0)  // GEMM1 gathers the routed rows through perm_token and the shared rows in order
+  if (!h_ready) {
+    x1.a = &xa; x1.b = &xgu; x1.out_map = &xho; x1.M = N; x1.out = hs_workspace; x1.b_planes = xplanes;
+  }
+  moe_status_t st = MOE_OK;
+  if (h_ready && Mr == 0)
+    ;  // nothing left for a first GEMM
+  else if (gather && Mr > 0)  // GEMM1 gathers the routed rows through perm_token and the shared rows in order
     st = gu ? tc::launch<2>(mgu, mgu, mgu, mho, offsets, G, Mr, D, F, h_workspace, status, s, xn, N, perm_token,
                             planes, x1)
             : tc::launch<2>(mg, mg, mu, mho, offsets, G, Mr, D, F, h_workspace, status, s, xn, N, perm_token, 0, x1);
@@ -1319,6 +1331,28 @@ extern "C" moe_status_t moe_grouped_swiglu_shared(const void* x_perm, const int3
   tc::ExtraGroup x2;
   x2.a = &xh; x2.b = &xd; x2.out_map = &xyo; x2.M = N; x2.out = shared_y; x2.b_planes = 0;
   return tc::launch<1>(mh, md, md, myo, offsets, G, Mr, F, D, y_perm, status, s, nullptr, 0, nullptr, 0, x2);
+}
+}  // namespace
+}  // namespace moe
+
+extern "C" moe_status_t moe_grouped_swiglu_shared(const void* x_perm, const int32_t* perm_token,
+                                                  const int32_t* offsets, int G, int M_total, int D, int F,
+                                                  const void* w_gate, const void* w_up, const void* w_down,
+                                                  void* h_workspace, void* y_perm, const void* xn, int N,
+                                                  const void* ws_gate, const void* ws_up, const void* ws_down,
+                                                  void* hs_workspace, void* shared_y, moe_stream_t stream) {
+  return moe::grouped_shared_impl(x_perm, perm_token, offsets, G, M_total, D, F, w_gate, w_up, w_down, h_workspace,
+                                  y_perm, xn, N, ws_gate, ws_up, ws_down, hs_workspace, shared_y, stream, false);
+}
+
+extern "C" moe_status_t moe_grouped_swiglu_shared_h(const void* x_perm, const int32_t* perm_token,
+                                                    const int32_t* offsets, int G, int M_total, int D, int F,
+                                                    const void* w_gate, const void* w_up, const void* w_down,
+                                                    void* h_workspace, void* y_perm, const void* xn, int N,
+                                                    const void* ws_down, void* hs_workspace, void* shared_y,
+                                                    moe_stream_t stream) {
+  return moe::grouped_shared_impl(x_perm, perm_token, offsets, G, M_total, D, F, w_gate, w_up, w_down, h_workspace,
+                                  y_perm, xn, N, nullptr, nullptr, ws_down, hs_workspace, shared_y, stream, true);
 }
 
 extern "C" moe_status_t moe_grouped_swiglu_gather(const void* xn, int N, const int32_t* perm_token,

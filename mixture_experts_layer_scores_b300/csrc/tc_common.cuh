@@ -262,6 +262,11 @@ bool make_map_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t col
 // planes) box brings the same rows of every plane, plane after plane.
 bool make_map_planes_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t planes,
                           uint32_t box_rows);
+// One map over a gate and an up projection ([rows, cols] each) addressed as two planes of one
+// tensor: a (64, box_rows, 2) box brings the same rows of both.  *planes = 1 when w_gate lies
+// below w_up (gate plane first), 2 otherwise; false when their distance does not allow it.
+bool make_map_gate_up(CUtensorMap* m, const void* w_gate, const void* w_up, uint64_t rows, uint64_t cols,
+                      uint32_t box_rows, int* planes);
 
 }  // namespace tc
 }  // namespace moe

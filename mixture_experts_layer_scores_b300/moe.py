@@ -26,7 +26,8 @@ EXPORTS = ("moe_status_string", "moe_last_device_status", "moe_version", "moe_ro
            "moe_permute_noalloc_max_scratch_bytes", "moe_router_split_bytes", "moe_router_split",
            "moe_router_topk_split", "moe_router_topk_split_workspace_bytes", "moe_permute_capacity",
            "moe_grouped_swiglu_gather", "moe_grouped_swiglu_ex", "moe_expert_capacity",
-           "moe_selftest_bounded_wait", "moe_permute_update_bias", "moe_grouped_swiglu_shared")
+           "moe_selftest_bounded_wait", "moe_permute_update_bias", "moe_grouped_swiglu_shared",
+           "moe_router_topk_split_shared", "moe_grouped_swiglu_shared_h")
 
 
 class MoEError(RuntimeError):
@@ -73,6 +74,10 @@ def load():
                                      vp, vp], i32),
         "moe_grouped_swiglu_shared": ([vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp,
                                        vp, vp], i32),
+        "moe_router_topk_split_shared": ([vp, i32, i32, vp, vp, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp, vp, i32,
+                                          vp, vp], i32),
+        "moe_grouped_swiglu_shared_h": ([vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp,
+                                         vp], i32),
     }
     for name, (args, res) in sig.items():
         f = getattr(L, name)
@@ -220,6 +225,46 @@ def moe_router_topk_split(xn, w_split, bias, k, score_fn="softmax", logits_out=N
         _p(xn), N, D, _p(w_split), _p(bias), E, k, SCORE_FN[score_fn], _p(logits_out), _p(topk_idx),
         _p(topk_gate), _p(near_tie), _p(workspace), workspace.numel(), _stream(stream)))
     return logits_out, topk_idx, topk_gate, near_tie
+
+
+def moe_router_topk_split_shared(xn, w_split, bias, k, shared, score_fn="softmax", logits_out=None, topk_idx=None,
+                                 topk_gate=None, near_tie=None, want_near_tie=True, workspace=None, hs_out=None,
+                                 stream=None):
+    """moe_router_topk_split and the shared expert's first GEMM (shared = (w_gate[1,F,D],
+    w_up[1,F,D], ...)) in one launch over the same token tiles.  Returns (logits, idx, gate,
+    near_tie, hs) with hs [N, F] bf16 the shared expert's H."""
+    L = load()
+    N, D = xn.shape
+    E = w_split.shape[1]
+    dev = xn.device
+    sg, su = shared[0], shared[1]
+    F = sg.shape[1]
+    _need("xn", xn, torch.bfloat16)
+    _need("w_split", w_split, torch.bfloat16, (3, E, D), dev)
+    _need("bias", bias, torch.float32, (E,), dev)
+    _need("shared w_gate", sg, torch.bfloat16, (1, F, D), dev)
+    _need("shared w_up", su, torch.bfloat16, (1, F, D), dev)
+    _need("logits_out", logits_out, torch.float32, (N, E), dev)
+    _need("topk_idx", topk_idx, torch.int32, (N, k), dev)
+    _need("topk_gate", topk_gate, torch.float32, (N, k), dev)
+    _need("near_tie", near_tie, torch.uint8, (N,), dev)
+    _need("workspace", workspace, device=dev)
+    _need("hs_out", hs_out, torch.bfloat16, (N, F), dev)
+    e = lambda *sh, dt: torch.empty(*sh, dtype=dt, device=dev)
+    logits_out = e(N, E, dt=torch.float32) if logits_out is None else logits_out
+    topk_idx = e(N, k, dt=torch.int32) if topk_idx is None else topk_idx
+    topk_gate = e(N, k, dt=torch.float32) if topk_gate is None else topk_gate
+    if near_tie is None and want_near_tie:
+        near_tie = e(N, dt=torch.uint8)
+    if workspace is None:
+        workspace = e(max(1, router_split_workspace_bytes(N, D, E)), dt=torch.uint8)
+    hs_out = e(N, F, dt=torch.bfloat16) if hs_out is None else hs_out
+    _cuda(xn, w_split, bias, sg, su, logits_out, topk_idx, topk_gate, near_tie, workspace, hs_out)
+    _chk("moe_router_topk_split_shared", L.moe_router_topk_split_shared(
+        _p(xn), N, D, _p(w_split), _p(bias), E, k, SCORE_FN[score_fn], _p(logits_out), _p(topk_idx),
+        _p(topk_gate), _p(near_tie), _p(workspace), workspace.numel(), _p(sg), _p(su), F, _p(hs_out),
+        _stream(stream)))
+    return logits_out, topk_idx, topk_gate, near_tie, hs_out
 
 
 def permute_workspace_bytes(N, k, E) -> int:
@@ -381,6 +426,41 @@ def moe_grouped_swiglu_shared(x_perm, offsets, w_gate, w_up, w_down, xn, shared,
     return y_perm, shared_y
 
 
+def moe_grouped_swiglu_shared_h(x_perm, offsets, w_gate, w_up, w_down, xn, w_down_shared, hs, y_perm=None,
+                                h_workspace=None, shared_y=None, stream=None, perm_token=None):
+    """moe_grouped_swiglu_shared when hs [N, F] already holds the shared expert's H (from
+    moe_router_topk_split_shared): the routed experts' SwiGLU and the shared expert's second
+    GEMM (w_down_shared [1, D, F]) in the routed GEMM2 launch.  Returns (y_perm, shared_y)."""
+    L = load()
+    G, F, D = w_gate.shape
+    M = perm_token.shape[0] if perm_token is not None else x_perm.shape[0]
+    N = hs.shape[0]
+    dt, dev = hs.dtype, hs.device
+    if perm_token is None and x_perm is None:
+        raise ValueError("x_perm or perm_token is needed")
+    _need("hs", hs, torch.bfloat16, (N, F))
+    _need("x_perm", x_perm, dt, (M, D), dev)
+    _need("perm_token", perm_token, torch.int32, (M,), dev)
+    _need("xn", xn, dt, (N, D), dev)
+    _need("offsets", offsets, torch.int32, (G + 1,), dev)
+    _need("w_gate", w_gate, dt, (G, F, D), dev)
+    _need("w_up", w_up, dt, (G, F, D), dev)
+    _need("w_down", w_down, dt, (G, D, F), dev)
+    _need("shared w_down", w_down_shared, dt, (1, D, F), dev)
+    _need("h_workspace", h_workspace, dt, (M, F), dev)
+    _need("y_perm", y_perm, dt, (M, D), dev)
+    _need("shared_y", shared_y, dt, (N, D), dev)
+    e = lambda *sh: torch.empty(*sh, dtype=dt, device=dev)
+    h_workspace = e(M, F) if h_workspace is None else h_workspace
+    y_perm = e(M, D) if y_perm is None else y_perm
+    shared_y = e(N, D) if shared_y is None else shared_y
+    _cuda(x_perm, perm_token, xn, offsets, w_gate, w_up, w_down, w_down_shared, hs, h_workspace, y_perm, shared_y)
+    _chk("moe_grouped_swiglu_shared_h", L.moe_grouped_swiglu_shared_h(
+        _p(x_perm), _p(perm_token), _p(offsets), G, M, D, F, _p(w_gate), _p(w_up), _p(w_down), _p(h_workspace),
+        _p(y_perm), _p(xn), N, _p(w_down_shared), _p(hs), _p(shared_y), _stream(stream)))
+    return y_perm, shared_y
+
+
 def moe_grouped_swiglu_gather(xn, perm_token, offsets, w_gate, w_up, w_down, h_workspace=None,
                               y_perm=None, stream=None):
     """Grouped SwiGLU whose row i reads xn[perm_token[i]] directly (bf16).  Returns y_perm."""
@@ -477,13 +557,19 @@ class MoELayer:
     """Top-k MoE FFN layer forward on one GPU, with reusable device buffers."""
 
     def __init__(self, weights: LayerWeights, N: int, k: int, score_fn="softmax", gamma=1e-3,
-                 dtype=torch.bfloat16, capacity_factor=None, gather=None, fuse_shared=True):
+                 dtype=torch.bfloat16, capacity_factor=None, gather=None, fuse_shared=True,
+                 router_shared=False):
         """gather (bf16): the first expert GEMM reads its rows from xn through perm_token
         instead of from a permuted copy, which is then never written; False writes x_perm in
         the permute and runs the GEMM on it.  None chooses by size: gathering costs the GEMM
         roughly a tenth of its first half, the copy moves (1 + k) N D bf16 values, so it
         gathers when d_ff * k / (k + 1) <= 1024 (measured: faster on the handbook and skewed
-        layers, slower on the Mixtral- and DeepSeek-V3-shaped ones)."""
+        layers, slower on the Mixtral- and DeepSeek-V3-shaped ones).
+        router_shared (bf16, shared expert with the routed d_ff): the shared expert's first
+        GEMM runs in the router's launch over the same token tiles and its second in the
+        routed GEMM2 launch (moe_router_topk_split_shared, moe_grouped_swiglu_shared_h); the
+        same outputs, bit for bit, as the default, where both of its GEMMs ride in the routed
+        launches."""
         w = weights
         self.w, self.k, self.score_fn, self.gamma = w, k, score_fn, gamma
         E = w.w_router.shape[0]
@@ -525,6 +611,9 @@ class MoELayer:
         # the shared expert's tiles ride in the routed experts' launches (same d_ff, bf16)
         self.fuse_shared = bool(fuse_shared) and w.shared is not None and dtype == torch.bfloat16 \
             and w.shared[0].shape[1] == self.F
+        self.router_shared = bool(router_shared) and self.fuse_shared and self.tc_router
+        if router_shared and not self.router_shared:
+            raise ValueError("router_shared needs bf16, a shared expert with the routed d_ff and fuse_shared")
 
     def forward(self, xn, h, update_bias=True, stream=None, out=None):
         """out = h + shared(xn) + sum_j gate_j Expert_j(xn), and the +-gamma bias step on
@@ -570,7 +659,11 @@ class MoELayer:
         """Every routed expert's SwiGLU FFN over its block of permuted rows -> y_perm (and the
         shared expert's -> sh_y, in the same launches, when fused)."""
         w = self.w
-        if self.fuse_shared:
+        if self.router_shared:  # sh_h came from the router's launch
+            moe_grouped_swiglu_shared_h(self.x_perm, self.offsets, w.w_gate, w.w_up, w.w_down, xn, w.shared[2],
+                                        self.sh_h, self.y_perm, self.h_ws, self.sh_y, stream=stream,
+                                        perm_token=self.perm_token if self.gather else None)
+        elif self.fuse_shared:
             moe_grouped_swiglu_shared(self.x_perm, self.offsets, w.w_gate, w.w_up, w.w_down, xn, w.shared,
                                       self.h_ws, self.y_perm, self.sh_h, self.sh_y, stream=stream,
                                       perm_token=self.perm_token if self.gather else None)
@@ -601,7 +694,12 @@ class MoELayer:
         """Router + top-k.  bf16 activations: the fp32 router weight is re-split into bf16
         planes (every call, so weight updates are always seen) and run on tensor cores."""
         w = self.w
-        if self.tc_router:
+        if self.router_shared:  # and the shared expert's first GEMM, over the same token tiles
+            moe_router_split(w.w_router, self.w_split, stream=stream)
+            moe_router_topk_split_shared(xn, self.w_split, w.bias, self.k, w.shared, self.score_fn, self.logits,
+                                         self.idx, self.gate, self.near_tie, workspace=self.router_ws,
+                                         hs_out=self.sh_h, stream=stream)
+        elif self.tc_router:
             moe_router_split(w.w_router, self.w_split, stream=stream)
             moe_router_topk_split(xn, self.w_split, w.bias, self.k, self.score_fn, self.logits,
                                   self.idx, self.gate, self.near_tie, workspace=self.router_ws,

@@ -77,6 +77,21 @@ def test_new_entry_points_reject_bad_arguments_before_launch(lib):
              None) == -1                                            # routed rows but no operands
     assert g(None, None, None, 4, 0, 128, 128, None, None, None, None, None, None, 8, None, None, None, None, None,
              None) == -1                                            # shared rows but no operands
+    r = raw.moe_router_topk_split_shared
+    r.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                  ctypes.c_int, ctypes.c_int] + [ctypes.c_void_p] * 5 + [ctypes.c_size_t, ctypes.c_void_p,
+                  ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
+    r.restype = ctypes.c_int
+    assert r(None, 16, 64, None, None, 8, 2, 0, None, None, None, None, None, 0, None, None, 64, None,
+             None) == -1                                            # no shared gate weights
+    h = raw.moe_grouped_swiglu_shared_h
+    h.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                  ctypes.c_int] + [ctypes.c_void_p] * 5 + [ctypes.c_void_p, ctypes.c_int] + [ctypes.c_void_p] * 4
+    h.restype = ctypes.c_int
+    assert h(None, None, None, 0, 0, 128, 128, None, None, None, None, None, None, 0, None, None, None,
+             None) == -1                                            # G < 1
+    assert h(None, None, None, 4, 0, 128, 128, None, None, None, None, None, None, 8, None, None, None,
+             None) == -1                                            # shared rows, no H or weights
 
 
 def test_expert_capacity_through_the_abi(lib):

@@ -188,3 +188,20 @@ def test_sustained_gemm_mode_runs_its_three_inputs():
     torch.cuda.synchronize()
     assert moe.last_device_status() == 0
     assert torch.equal(out0, out1)
+
+
+def test_full_size_router_launch_with_the_shared_first_gemm():
+    """DeepSeek-V3-shaped layer with the shared expert's first GEMM in the router's launch: the
+    default layer's routing, shared H and output, bit for bit, at full size."""
+    cfg = synth.CONFIGS["deepseek_v3"]
+    layer, xn, h, b0, out = _layer(cfg, cfg.k)
+    out_ref = out.clone()
+    w = layer.w
+    lw = moe.LayerWeights(w.w_router, b0.clone(), w.w_gate, w.w_up, w.w_down, w.shared)
+    got = moe.MoELayer(lw, cfg.N, cfg.k, cfg.score_fn, cfg.gamma, router_shared=True)
+    o = got.forward(xn, h)
+    torch.cuda.synchronize()
+    assert moe.last_device_status() == 0
+    assert torch.equal(got.idx, layer.idx) and torch.equal(got.logits, layer.logits)
+    assert torch.equal(got.sh_h, layer.sh_h) and torch.equal(got.sh_y, layer.sh_y)
+    assert torch.equal(o, out_ref)

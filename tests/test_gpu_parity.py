@@ -430,6 +430,38 @@ def test_shared_expert_in_routed_launches(N, D, E, F, k, gather):
         P.assert_close("shared_y", P.np64(sh_y.cpu()), want)
 
 
+@pytest.mark.parametrize("gather", [False, True], ids=["copy", "gather"])
+@pytest.mark.parametrize("N,D,E,F,k", [(333, 512, 32, 256, 8), (200, 256, 256, 128, 8), (300, 256, 896, 256, 16),
+                                       (1000, 320, 64, 192, 4)],
+                         ids=["E32", "E256-splitK", "E896-k16", "F192"])
+def test_router_launch_runs_the_shared_first_gemm(N, D, E, F, k, gather):
+    """MoELayer(router_shared=True): the shared expert's first GEMM in the router's launch
+    (moe_router_topk_split_shared) and its second in the routed GEMM2 launch
+    (moe_grouped_swiglu_shared_h) give the default layer's logits, ids, gates, shared H and
+    output bit for bit, and the oracle's shared expert."""
+    cfg = synth.scaled(C["deepseek_v3"], N=N, D=D, E=E, F=F, k=k, F_shared=F)
+    gi = P.make_inputs(cfg, "cuda")
+    lw = lambda: moe.LayerWeights(gi["w_router"], gi["bias"].clone(), gi["w_gate"], gi["w_up"], gi["w_down"],
+                                  gi["shared"])
+    ref = moe.MoELayer(lw(), cfg.N, cfg.k, cfg.score_fn, cfg.gamma, gather=gather)
+    got = moe.MoELayer(lw(), cfg.N, cfg.k, cfg.score_fn, cfg.gamma, gather=gather, router_shared=True)
+    assert got.router_shared and not ref.router_shared and ref.fuse_shared
+    o_ref = ref.forward(gi["xn"], gi["h"]).clone()
+    o_got = got.forward(gi["xn"], gi["h"])
+    torch.cuda.synchronize()
+    assert moe.last_device_status() == 0
+    for name in ("logits", "idx", "gate", "near_tie", "sh_h", "sh_y", "y_perm"):
+        a, b = getattr(ref, name), getattr(got, name)
+        if name == "y_perm":
+            kept = int(ref.offsets[-1])
+            a, b = a[:kept], b[:kept]
+        assert torch.equal(a, b), name
+    assert torch.equal(o_ref, o_got)
+    xc = P.np64(gi["xn"].cpu())
+    want = moe_oracle.swiglu_expert(xc, *(P.np64(t[0].cpu()) for t in gi["shared"]))
+    P.assert_close("shared_y", P.np64(got.sh_y.cpu()), want)
+
+
 def test_gather_repeated_back_to_back():
     """The gathering GEMM1 with CTA-pair GEMM2 (experts averaging >= 256 rows), 30 calls back
     to back: every call bit-identical to the copy path, no device status raised (the CTAs of a
