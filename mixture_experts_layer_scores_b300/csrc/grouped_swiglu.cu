@@ -963,12 +963,14 @@ moe_status_t launch_pair(const CUtensorMap& a, const CUtensorMap& a_half, const 
 
 namespace simt {
 
-// fp32 grouped SwiGLU on CUDA cores: 64 x 64 output tiles, 256 threads with 4 x 4 outputs
-// each, 32-wide K slices staged in shared memory (k-major, so a thread reads four rows or
-// four columns as one float4), the next slice loaded into registers during the FMAs.  Every output is one fp32 FMA chain over K in index order
-// (bit-identical to a plain dot-product loop).  Tiles are (group, 64-row block, column
-// block); a CTA finds its group by walking the offsets.
-constexpr int TM = 64, TN = 64, TK = 32, PAD = 4;
+// fp32 grouped SwiGLU on CUDA cores: 32 x 64 output tiles, 256 threads with 2 x 4 outputs
+// each (two rows of four columns: a small layer still gets several warps per SM), 32-wide K
+// slices staged in shared memory (k-major, so a thread reads its two rows as one float2 and
+// four columns as one float4), the next slice loaded into registers during the FMAs.  Every
+// output is one fp32 FMA chain over K in index order (bit-identical to a plain dot-product
+// loop).  Tiles are (group, 32-row block, column block); a CTA finds its group by walking
+// the offsets.
+constexpr int TM = 32, TN = 64, TK = 32, PAD = 4;
 
 struct SimtTile {
   int g, row0, rows, col0;
@@ -997,24 +999,25 @@ __device__ __forceinline__ SimtTile simt_tile(int t, const int32_t* __restrict__
   return r;
 }
 
-// One thread's share of a 64-row x TK-column slice of a row-major [*, ld] matrix (rows
-// [row0, row0 + rows), columns [k0, k0 + TK); zero beyond `rows`): TM * TK / 4 / 256 float4.
-constexpr int SLICE_V = TM * TK / 4 / 256;
+// One thread's share of a ROWS-row x TK-column slice of a row-major [*, ld] matrix (rows
+// [row0, row0 + rows), columns [k0, k0 + TK); zero beyond `rows`): ROWS * TK / 4 / 256 float4.
+template <int ROWS>
 struct Slice {
-  float4 v[SLICE_V];
+  static constexpr int V = ROWS * TK / 4 / 256;
+  float4 v[V];
   __device__ __forceinline__ void load(const float* __restrict__ src, int ld, int row0, int rows, int k0) {
 #pragma unroll
-    for (int q = 0; q < SLICE_V; ++q) {
+    for (int q = 0; q < V; ++q) {
       const int i = threadIdx.x + q * 256;
       const int m = i / (TK / 4), kq = (i % (TK / 4)) * 4;
       v[q] = m < rows ? *reinterpret_cast<const float4*>(src + (size_t)(row0 + m) * ld + k0 + kq)
                       : make_float4(0.f, 0.f, 0.f, 0.f);
     }
   }
-  // into dst[k][m] (k-major, so the compute loop reads four rows or columns as one float4)
-  __device__ __forceinline__ void store(float (*dst)[TM + PAD]) const {
+  // into dst[k][m] (k-major, so the compute loop reads rows or columns as one vector)
+  __device__ __forceinline__ void store(float (*dst)[ROWS + PAD]) const {
 #pragma unroll
-    for (int q = 0; q < SLICE_V; ++q) {
+    for (int q = 0; q < V; ++q) {
       const int i = threadIdx.x + q * 256;
       const int m = i / (TK / 4), kq = (i % (TK / 4)) * 4;
       dst[kq + 0][m] = v[q].x;
@@ -1040,8 +1043,9 @@ __global__ void __launch_bounds__(256, 2) swiglu_up_kernel(const float* __restri
   const int ncols = min(TN, F - tl.col0);
   const float* wgg = wg + ((size_t)tl.g * F + tl.col0) * D;
   const float* wug = wu + ((size_t)tl.g * F + tl.col0) * D;
-  float ag[4][4] = {}, au[4][4] = {};
-  Slice sx, sg, su;
+  float ag[2][4] = {}, au[2][4] = {};
+  Slice<TM> sx;
+  Slice<TN> sg, su;
   sx.load(x, D, tl.row0, tl.rows, 0);
   sg.load(wgg, D, 0, ncols, 0);
   su.load(wug, D, 0, ncols, 0);
@@ -1057,12 +1061,12 @@ __global__ void __launch_bounds__(256, 2) swiglu_up_kernel(const float* __restri
     }
 #pragma unroll 8
     for (int k = 0; k < TK; ++k) {
-      const float4 a = *reinterpret_cast<const float4*>(&xs[k][ty * 4]);
+      const float2 a = *reinterpret_cast<const float2*>(&xs[k][ty * 2]);
       const float4 b = *reinterpret_cast<const float4*>(&gs[k][tx * 4]);
       const float4 c = *reinterpret_cast<const float4*>(&us[k][tx * 4]);
-      const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w}, cv[4] = {c.x, c.y, c.z, c.w};
+      const float av[2] = {a.x, a.y}, bv[4] = {b.x, b.y, b.z, b.w}, cv[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+      for (int i = 0; i < 2; ++i)
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           ag[i][j] = fmaf(av[i], bv[j], ag[i][j]);
@@ -1072,8 +1076,8 @@ __global__ void __launch_bounds__(256, 2) swiglu_up_kernel(const float* __restri
     __syncthreads();
   }
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int r = ty * 4 + i;
+  for (int i = 0; i < 2; ++i) {
+    const int r = ty * 2 + i;
     if (r >= tl.rows) continue;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -1099,8 +1103,9 @@ __global__ void __launch_bounds__(256, 2) swiglu_down_kernel(const float* __rest
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
   const int ncols = min(TN, D - tl.col0);
   const float* wdg = wd + ((size_t)tl.g * D + tl.col0) * F;
-  float acc[4][4] = {};
-  Slice sh, sd;
+  float acc[2][4] = {};
+  Slice<TM> sh;
+  Slice<TN> sd;
   sh.load(h, F, tl.row0, tl.rows, 0);
   sd.load(wdg, F, 0, ncols, 0);
   for (int k0 = 0; k0 < F; k0 += TK) {
@@ -1113,19 +1118,19 @@ __global__ void __launch_bounds__(256, 2) swiglu_down_kernel(const float* __rest
     }
 #pragma unroll 8
     for (int k = 0; k < TK; ++k) {
-      const float4 a = *reinterpret_cast<const float4*>(&hs[k][ty * 4]);
+      const float2 a = *reinterpret_cast<const float2*>(&hs[k][ty * 2]);
       const float4 b = *reinterpret_cast<const float4*>(&ds[k][tx * 4]);
-      const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+      const float av[2] = {a.x, a.y}, bv[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+      for (int i = 0; i < 2; ++i)
 #pragma unroll
         for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
     }
     __syncthreads();
   }
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int r = ty * 4 + i;
+  for (int i = 0; i < 2; ++i) {
+    const int r = ty * 2 + i;
     if (r >= tl.rows) continue;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {

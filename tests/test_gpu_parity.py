@@ -25,6 +25,7 @@ CASES = {
     "bf16_zipf_skewed": synth.scaled(C["skewed"], N=1024, D=256, E=64, F=128, k=8),
     "bf16_long_K": synth.scaled(C["handbook"], N=300, D=1024, E=8, F=640, k=2),
     "f32_tiny_full_size": C["tiny"],
+    "f32_ragged": synth.scaled(C["tiny"], N=301, D=320, E=8, F=192, k=3),
     "bf16_sqrt_softplus": synth.scaled(C["handbook"], N=400, D=256, E=32, F=128, k=4, score_fn="sqrt_softplus"),
     # d_ff = 256: with bf16 H and Y an exact bf16 pipeline itself reaches max|err| = 4.1e-2 * rms
     # at d_ff = 64 (2.7e-2 at 128, 2.0e-2 at 256), so the 3e-2 bound needs d_ff >= ~128
