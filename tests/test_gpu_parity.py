@@ -30,6 +30,8 @@ CASES = {
     # d_ff = 256: with bf16 H and Y an exact bf16 pipeline itself reaches max|err| = 4.1e-2 * rms
     # at d_ff = 64 (2.7e-2 at 128, 2.0e-2 at 256), so the 3e-2 bound needs d_ff >= ~128
     "bf16_E896_k16_shared": synth.scaled(C["deepseek_v3"], N=300, D=256, E=896, F=256, k=16, F_shared=256),
+    # the largest expert count: most of the 1024 experts get no or one row
+    "bf16_E1024_k8_shared": synth.scaled(C["deepseek_v3"], N=256, D=256, E=1024, F=128, k=8, F_shared=128),
 }
 
 
@@ -238,6 +240,38 @@ def test_capacity_dropping(factor):
                   P.np64(ci["h"])[all_kept])
     print("capacity factor", factor, "capacity", cap, "dropped slots", dropped, "of", cfg.N * cfg.k,
           "tokens with no slot kept", int(none_kept.sum()))
+
+
+@pytest.mark.parametrize("router_shared", [False, True], ids=["shared-in-gemm", "shared-in-router"])
+def test_capacity_with_a_shared_expert(router_shared):
+    """Expert capacity on the DeepSeek-V3 recipe (sigmoid router, shared expert): the kept rows,
+    dropped slots, counts and offsets match the oracle, and the output does too -- a token
+    that lost every routed slot gets its residual plus the shared expert's output -- with the
+    shared expert's first GEMM in the routed launch or in the router's."""
+    cfg = synth.scaled(C["deepseek_v3"], N=512, D=256, E=32, F=128, k=8, F_shared=128)
+    cap = moe.expert_capacity(0.75, cfg.N, cfg.k, cfg.E)
+    b = _bias(cfg, 0.05 * 0.05)
+    gi = P.make_inputs(cfg, "cuda", b)
+    L = moe.MoELayer(moe.LayerWeights(gi["w_router"], gi["bias"].clone(), gi["w_gate"], gi["w_up"], gi["w_down"],
+                                      gi["shared"]), cfg.N, cfg.k, cfg.score_fn, cfg.gamma, capacity_factor=0.75,
+                     router_shared=router_shared)
+    out = L.forward(gi["xn"], gi["h"])
+    torch.cuda.synchronize()
+    assert moe.last_device_status() == 0
+    ci = P.make_inputs(cfg, "cpu", b)
+    sh = tuple(P.np64(t) for t in ci["shared"])
+    o = moe_oracle.moe_layer(P.np64(ci["xn"]), P.np64(ci["h"]), ci["w_router"].numpy(), ci["bias"].numpy(),
+                             P.np64(ci["w_gate"]), P.np64(ci["w_up"]), P.np64(ci["w_down"]), cfg.k, cfg.score_fn,
+                             shared=sh, gamma=cfg.gamma, capacity=cap)
+    same = ~(L.idx.cpu().numpy() != o["idx"]).any(1)
+    assert same.mean() > 0.95
+    if same.all():
+        assert np.array_equal(L.counts.cpu().numpy(), o["counts"])
+        assert np.array_equal(L.offsets.cpu().numpy(), o["offsets"])
+        assert np.array_equal(L.row_map.cpu().numpy(), o["row_map"])
+    assert (L.row_map.cpu().numpy() < 0).any()  # some slots dropped
+    P.assert_close("shared_y", P.np64(L.sh_y.cpu()), o["shared_y"])
+    P.assert_close("out (same routing)", P.np64(out.cpu())[same], o["out"][same])
 
 
 def test_gather_rejects_bad_token_index():
