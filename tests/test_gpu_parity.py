@@ -345,13 +345,19 @@ def test_grouped_gemm_cta_cap_keeps_bits(name):
             assert torch.equal(h_ws, ref[0]) and torch.equal(y, ref[1]), cap
 
 
-def test_captured_forward_matches_eager():
+@pytest.mark.parametrize("variant", ["plain", "shared", "shared-in-router"])
+def test_captured_forward_matches_eager(variant):
     """A CUDA graph of the whole layer (MoELayer.capture) replays the same kernels: outputs and
-    the evolving bias equal an eager forward's, bit for bit, over several steps."""
-    cfg = synth.scaled(C["handbook"], N=256, D=256, E=16, F=128, k=4)
+    the evolving bias equal an eager forward's, bit for bit, over several steps -- also with a
+    shared expert, in the routed launches or with its first GEMM in the router's launch."""
+    if variant == "plain":
+        cfg = synth.scaled(C["handbook"], N=256, D=256, E=16, F=128, k=4)
+    else:
+        cfg = synth.scaled(C["deepseek_v3"], N=256, D=256, E=32, F=128, k=8, F_shared=128)
     gi = P.make_inputs(cfg, "cuda")
     mk = lambda: moe.MoELayer(moe.LayerWeights(gi["w_router"], gi["bias"].clone(), gi["w_gate"], gi["w_up"],
-                                               gi["w_down"], None), cfg.N, cfg.k, cfg.score_fn, cfg.gamma)
+                                               gi["w_down"], gi["shared"]), cfg.N, cfg.k, cfg.score_fn, cfg.gamma,
+                              router_shared=variant == "shared-in-router")
     eager, graphed = mk(), mk()
     xn, h = gi["xn"].clone(), gi["h"].clone()
     # one eager warm-up call each: the library sets itself up outside the capture
