@@ -473,8 +473,8 @@ def test_shared_expert_in_routed_launches(N, D, E, F, k, gather):
 
 @pytest.mark.parametrize("gather", [False, True], ids=["copy", "gather"])
 @pytest.mark.parametrize("N,D,E,F,k", [(333, 512, 32, 256, 8), (200, 256, 256, 128, 8), (300, 256, 896, 256, 16),
-                                       (1000, 320, 64, 192, 4)],
-                         ids=["E32", "E256-splitK", "E896-k16", "F192"])
+                                       (1000, 320, 64, 192, 4), (2048, 256, 8, 128, 2)],
+                         ids=["E32", "E256-splitK", "E896-k16", "F192", "pair-routed"])
 def test_router_launch_runs_the_shared_first_gemm(N, D, E, F, k, gather):
     """MoELayer(router_shared=True): the shared expert's first GEMM in the router's launch
     (moe_router_topk_split_shared) and its second in the routed GEMM2 launch
